@@ -1,0 +1,162 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+``cpu_baseline`` / reference leg may import this package.  It shares no code
+with the CUDA library in ``io_aware_exact_gb300``: the arithmetic lives in
+``attn_oracle.c`` (plain C, fp64), built by :func:`build` with the host
+compiler, and this module only marshals numpy arrays into it.
+
+The functions follow, one head at a time:
+
+* sj-techlog "FlashAttention 원 논문 해부", section "원 논문의 정의":
+  S = tau Q K^T, P = softmax(S), O = P V, causal s_ij = -inf for j > i;
+* wonbeomjang.kr FlashAttention-2 review, "개선 2: m과 l 대신 L만 저장":
+  lse_i = m_i + log l_i (natural log, tau inside S);
+* same review, "Backward Pass": dV = P^T dO, dP = dO V^T,
+  dS_ij = P_ij (dP_ij - D_i), D_i = sum_j P_ij dP_ij, and (with tau inside S)
+  dQ = tau dS K, dK = tau dS^T Q.
+
+Parity status: every function here is pinned by tests in
+``tests/test_oracle_pins.py`` (page-printed worked examples, closed forms,
+invariants and finite differences); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``liboracle.so`` (OpenMP if available)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int64)
+            i64, ci, cd = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+            lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, cd,
+                                                 ip, i64, dp, dp]
+            lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, ci, cd,
+                                                 ip, i64, dp, dp, dp]
+            lib.oracle_attn_bwd_cols.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
+                                                 ci, cd, ip, i64, dp, dp]
+            for f in (lib.oracle_attn_fwd_rows, lib.oracle_attn_bwd_rows,
+                      lib.oracle_attn_bwd_cols):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _idx(sel, n) -> np.ndarray:
+    if sel is None:
+        return np.arange(n, dtype=np.int64)
+    return np.ascontiguousarray(np.asarray(sel, dtype=np.int64).reshape(-1))
+
+
+def _p(a):
+    if a.dtype == np.int64:
+        return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def attention_forward(q, k, v, causal: bool, scale: float, rows=None):
+    """O and lse of one head for the selected query rows (all by default).
+
+    q [nq, d], k [nk, d], v [nk, dv] (any float dtype; upcast exactly to fp64).
+    Returns (o [len(rows), dv], lse [len(rows)]), fp64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nq, d = q.shape
+    nk, dv = v.shape
+    assert k.shape == (nk, d)
+    r = _idx(rows, nq)
+    o = np.empty((r.size, dv), np.float64)
+    lse = np.empty((r.size,), np.float64)
+    rc = _load().oracle_attn_fwd_rows(_p(q), _p(k), _p(v), nq, nk, d, dv, int(bool(causal)),
+                                      float(scale), _p(r), r.size, _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_rows rejected its arguments")
+    return o, lse
+
+
+def attention_backward_rows(q, k, v, dO, causal: bool, scale: float, rows=None):
+    """(lse, D, dQ) of one head for the selected query rows (all by default)."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    nq, d = q.shape
+    nk, dv = v.shape
+    assert k.shape == (nk, d) and dO.shape == (nq, dv)
+    r = _idx(rows, nq)
+    lse = np.empty((r.size,), np.float64)
+    D = np.empty((r.size,), np.float64)
+    dq = np.empty((r.size, d), np.float64)
+    rc = _load().oracle_attn_bwd_rows(_p(q), _p(k), _p(v), _p(dO), nq, nk, d, dv,
+                                      int(bool(causal)), float(scale), _p(r), r.size,
+                                      _p(lse), _p(D), _p(dq))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_rows rejected its arguments")
+    return lse, D, dq
+
+
+def attention_backward_cols(q, k, v, dO, lse_all, D_all, causal: bool, scale: float,
+                            cols=None):
+    """(dK, dV) of one head for the selected key columns (all by default).
+
+    ``lse_all`` and ``D_all`` must be the oracle's own values for every row.
+    """
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    lse_all, D_all = _f64(lse_all), _f64(D_all)
+    nq, d = q.shape
+    nk, dv = v.shape
+    assert lse_all.shape == (nq,) and D_all.shape == (nq,)
+    c = _idx(cols, nk)
+    dk = np.empty((c.size, d), np.float64)
+    dvo = np.empty((c.size, dv), np.float64)
+    rc = _load().oracle_attn_bwd_cols(_p(q), _p(k), _p(v), _p(dO), _p(lse_all), _p(D_all),
+                                      nq, nk, d, dv, int(bool(causal)), float(scale),
+                                      _p(c), c.size, _p(dk), _p(dvo))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_cols rejected its arguments")
+    return dk, dvo
+
+
+def attention_backward(q, k, v, dO, causal: bool, scale: float):
+    """Full backward of one head: (dQ, dK, dV, lse, D), fp64."""
+    lse, D, dq = attention_backward_rows(q, k, v, dO, causal, scale)
+    dk, dv = attention_backward_cols(q, k, v, dO, lse, D, causal, scale)
+    return dq, dk, dv, lse, D

@@ -1,0 +1,306 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by mathematics.
+
+Nothing here compares the oracle with itself.  Each test ties it to something
+independent: values a page prints for a worked example (fixtures under
+``tests/golden/``), closed forms, invariants of softmax attention, an
+independently written online-softmax recurrence, and central finite
+differences of the forward for the backward.  The mistakes these are meant to
+catch include a dropped softmax scale, a transposed operand, a wrong causal
+boundary (j < i instead of j <= i), a missing max-subtraction, a wrong sign in
+dS and a wrong D.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# Page-printed worked examples
+# --------------------------------------------------------------------------
+
+def test_merge_worked_example():
+    """sj-techlog page, section "12살 숫자 예": fold new scores [3,1] (values
+    [10,20]) into the state m=2, l=1.5, u=6.  Two earlier keys with scores 2 and
+    2+ln(1/2) and values 6 and 0 produce exactly that state, so the whole row
+    is the four keys together and the oracle's O, lse must give the printed
+    l', u', o'."""
+    g = _golden("page1_merge_example.json")
+    st, new, pr, rnd = g["state_before"], g["new_tile"], g["printed"], g["printed_rounding"]
+    prev_scores = [st["m"], st["m"] + math.log(0.5)]
+    prev_values = [st["u"], 0.0]
+    # the constructed earlier keys reproduce the printed state exactly
+    o_prev, lse_prev = oracle.attention_forward([[1.0]], [[s] for s in prev_scores],
+                                                [[x] for x in prev_values], False, 1.0)
+    assert abs(lse_prev[0] - (st["m"] + math.log(st["l"]))) < 1e-14
+    assert abs(o_prev[0, 0] - st["u"] / st["l"]) < 1e-14
+
+    # the new tile alone: printed tilde_l, tilde_u
+    o_t, lse_t = oracle.attention_forward([[1.0]], [[s] for s in new["scores"]],
+                                          [[x] for x in new["values"]], False, 1.0)
+    l_t = math.exp(lse_t[0] - max(new["scores"]))
+    assert abs(l_t - pr["tilde_l"]) < 1e-4
+    assert abs(o_t[0, 0] * l_t - pr["tilde_u"]) < 1e-4
+
+    scores = prev_scores + new["scores"]
+    values = prev_values + new["values"]
+    o, lse = oracle.attention_forward([[1.0]], [[s] for s in scores], [[x] for x in values],
+                                      False, 1.0)
+    l_new = math.exp(lse[0] - pr["m_new"])
+    assert abs(l_new - pr["l_new"]) <= rnd["l_new"]
+    assert abs(o[0, 0] * l_new - pr["u_new"]) <= rnd["u_new"]
+    assert abs(o[0, 0] - pr["o_new"]) <= rnd["o_new"]
+
+
+def test_n5_example_printed_values():
+    """sj-techlog page, section "직접 검증과 재현": causal row 0 is [1, 0], and
+    row 4's running (m, l) after key blocks [0,2), [0,4), [0,5) are printed;
+    m + ln l is the log-normaliser over those keys."""
+    g = _golden("page1_n5_example.json")
+    q, k, v = (np.array(g[x], dtype=np.float64) for x in ("q", "k", "v"))
+    tau = 1.0 / math.sqrt(q.shape[1])
+    o, _ = oracle.attention_forward(q, k, v, True, tau)
+    assert np.array_equal(o[0], np.array(g["printed"]["causal_row0_output"]))
+    for st in g["printed"]["row4_block2_states"]:
+        end = st["keys"][1]
+        _, lse = oracle.attention_forward(q, k[:end], v[:end], False, tau, rows=[4])
+        want = st["m"] + math.log(st["l"])
+        assert abs(lse[0] - want) < 2e-6, (end, lse[0], want)
+        # row 4 sees every key, so causal and non-causal agree on it
+        _, lse_c = oracle.attention_forward(q, k, v, True, tau, rows=[4])
+        if end == 5:
+            assert abs(lse_c[0] - want) < 2e-6
+
+
+def _online_recurrence(q, k, v, tau, causal, block):
+    """Independent restatement of the tile-by-tile recurrence (sj-techlog page,
+    section "두 tile을 한 row로 합치는 식"), used only as a second algorithm."""
+    nq, nk = q.shape[0], k.shape[0]
+    out = np.zeros((nq, v.shape[1]))
+    lse = np.zeros(nq)
+    for i in range(nq):
+        m, l, u = -np.inf, 0.0, np.zeros(v.shape[1])
+        for start in range(0, nk, block):
+            idx = [j for j in range(start, min(start + block, nk)) if not causal or j <= i]
+            if not idx:
+                continue
+            s = np.array([tau * float(np.dot(q[i], k[j])) for j in idx])
+            mt = s.max()
+            lt = np.exp(s - mt).sum()
+            ut = (np.exp(s - mt)[:, None] * v[idx]).sum(axis=0)
+            mn = max(m, mt)
+            a = 0.0 if m == -np.inf else math.exp(m - mn)
+            b = math.exp(mt - mn)
+            l, u, m = a * l + b * lt, a * u + b * ut, mn
+        out[i] = u / l
+        lse[i] = m + math.log(l)
+    return out, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block", [1, 2, 3])
+def test_n5_example_tiled_equals_standard(causal, block):
+    """The page reports tiled == standard within 1e-12 for block sizes 1, 2, 3
+    on its N=5 inputs, causal and not."""
+    g = _golden("page1_n5_example.json")
+    q, k, v = (np.array(g[x], dtype=np.float64) for x in ("q", "k", "v"))
+    tau = 1.0 / math.sqrt(3.0)
+    o, lse = oracle.attention_forward(q, k, v, causal, tau)
+    o2, lse2 = _online_recurrence(q, k, v, tau, causal, block)
+    assert np.max(np.abs(o - o2)) <= g["printed"]["tiled_equals_standard_tol"]
+    assert np.max(np.abs(lse - lse2)) <= 1e-12
+
+
+def test_random_tiled_equals_standard():
+    r = _rng(1)
+    q, k, v = r.normal(size=(9, 4)), r.normal(size=(11, 4)), r.normal(size=(11, 3))
+    for causal in (False, True):
+        o, lse = oracle.attention_forward(q, k, v, causal, 0.8)
+        o2, lse2 = _online_recurrence(q, k, v, 0.8, causal, 4)
+        assert np.max(np.abs(o - o2)) < 1e-12 and np.max(np.abs(lse - lse2)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Closed forms and invariants of the forward
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_of_p_sum_to_one(causal):
+    """With V = 1 every output entry equals the row sum of P, which is 1."""
+    r = _rng(2)
+    q, k = 3 * r.normal(size=(13, 6)), 3 * r.normal(size=(13, 6))
+    o, _ = oracle.attention_forward(q, k, np.ones((13, 2)), causal, 1 / math.sqrt(6))
+    assert np.max(np.abs(o - 1.0)) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(causal):
+    """Adding w to every key adds tau q_i.w to all of row i's scores: O is
+    unchanged (softmax shift invariance) and lse shifts by exactly tau q_i.w."""
+    r = _rng(3)
+    q, k, v = r.normal(size=(10, 5)), r.normal(size=(10, 5)), r.normal(size=(10, 4))
+    w = r.normal(size=5)
+    tau = 0.6
+    o, lse = oracle.attention_forward(q, k, v, causal, tau)
+    o2, lse2 = oracle.attention_forward(q, k + w, v, causal, tau)
+    assert np.max(np.abs(o - o2)) < 1e-12
+    assert np.max(np.abs(lse2 - lse - tau * q @ w)) < 1e-12
+
+
+def test_key_value_permutation_equivariance():
+    r = _rng(4)
+    q, k, v = r.normal(size=(7, 4)), r.normal(size=(12, 4)), r.normal(size=(12, 3))
+    perm = r.permutation(12)
+    o, lse = oracle.attention_forward(q, k, v, False, 0.5)
+    o2, lse2 = oracle.attention_forward(q, k[perm], v[perm], False, 0.5)
+    assert np.max(np.abs(o - o2)) < 1e-12 and np.max(np.abs(lse - lse2)) < 1e-12
+
+
+def test_zero_query_gives_mean_and_log_count():
+    """Q = 0 makes all visible scores equal: O is the (prefix) mean of V and
+    lse is ln of the number of visible keys."""
+    r = _rng(5)
+    n = 9
+    k, v = r.normal(size=(n, 4)), r.normal(size=(n, 3))
+    q = np.zeros((n, 4))
+    o, lse = oracle.attention_forward(q, k, v, False, 0.5)
+    assert np.max(np.abs(o - v.mean(axis=0))) < 1e-12
+    assert np.max(np.abs(lse - math.log(n))) < 1e-12
+    o, lse = oracle.attention_forward(q, k, v, True, 0.5)
+    for i in range(n):
+        assert np.max(np.abs(o[i] - v[: i + 1].mean(axis=0))) < 1e-12
+        assert abs(lse[i] - math.log(i + 1)) < 1e-12
+
+
+def test_large_margin_key_selects_one_value_row():
+    d = 8
+    k = np.eye(d)
+    r = _rng(6)
+    v = r.normal(size=(d, 5))
+    sel = [3, 0, 7, 5]
+    q = np.stack([1000.0 * np.eye(d)[j] for j in sel])
+    o, _ = oracle.attention_forward(q, k, v, False, 1 / math.sqrt(d))
+    assert np.max(np.abs(o - v[sel])) < 1e-12
+
+
+def test_causal_first_row_is_first_value():
+    r = _rng(7)
+    q, k, v = 5 * r.normal(size=(6, 4)), 5 * r.normal(size=(6, 4)), r.normal(size=(6, 4))
+    o, lse = oracle.attention_forward(q, k, v, True, 0.5)
+    assert np.array_equal(o[0], v[0])
+    assert abs(lse[0] - 0.5 * float(q[0] @ k[0])) < 1e-12
+
+
+def test_huge_scores_do_not_overflow():
+    """Scores around 1e4 overflow exp() unless the row max is subtracted."""
+    r = _rng(8)
+    q, k, v = 100 * r.normal(size=(6, 4)), 100 * r.normal(size=(6, 4)), r.normal(size=(6, 2))
+    o, lse = oracle.attention_forward(q, k, v, False, 1.0)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert np.max(np.abs(o - oracle.attention_forward(q, k + 3.0, v, False, 1.0)[0])) < 1e-9
+
+
+def test_row_subset_matches_full():
+    r = _rng(9)
+    q, k, v = r.normal(size=(20, 4)), r.normal(size=(20, 4)), r.normal(size=(20, 4))
+    o, lse = oracle.attention_forward(q, k, v, True, 0.5)
+    rows = [19, 0, 7, 7]
+    o2, lse2 = oracle.attention_forward(q, k, v, True, 0.5, rows=rows)
+    assert np.array_equal(o2, o[rows]) and np.array_equal(lse2, lse[rows])
+
+
+def test_bad_rows_rejected():
+    z = np.zeros((3, 2))
+    with pytest.raises(ValueError):
+        oracle.attention_forward(z, z, z, False, 1.0, rows=[3])
+
+
+# --------------------------------------------------------------------------
+# Backward
+# --------------------------------------------------------------------------
+
+def _loss(q, k, v, dO, causal, tau):
+    o, _ = oracle.attention_forward(q, k, v, causal, tau)
+    return float(np.sum(o * dO))
+
+
+def _fd_grad(x, f, h=1e-6):
+    g = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        g[idx] = (f(xp) - f(xm)) / (2 * h)
+    return g
+
+
+@pytest.mark.parametrize("causal,nq,nk", [(False, 5, 5), (True, 5, 5), (False, 4, 6),
+                                          (True, 6, 4)])
+def test_backward_matches_finite_differences(causal, nq, nk):
+    """Central differences of L = sum(dO * O) w.r.t. every entry of Q, K, V.
+    tau = 0.7 is neither 1 nor 1/sqrt(d), so a dropped scale shows; d != dv
+    and nq != nk catch transposed operands."""
+    r = _rng(10 + nq + nk + int(causal))
+    d, dv, tau = 3, 2, 0.7
+    q, k, v = r.normal(size=(nq, d)), r.normal(size=(nk, d)), r.normal(size=(nk, dv))
+    dO = r.normal(size=(nq, dv))
+    dq, dk, dvv, _, _ = oracle.attention_backward(q, k, v, dO, causal, tau)
+    gq = _fd_grad(q, lambda x: _loss(x, k, v, dO, causal, tau))
+    gk = _fd_grad(k, lambda x: _loss(q, x, v, dO, causal, tau))
+    gv = _fd_grad(v, lambda x: _loss(q, k, x, dO, causal, tau))
+    for got, want in ((dq, gq), (dk, gk), (dvv, gv)):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_identities(causal):
+    """D_i = rowsum(dO o O); sum_j dS_ij = 0 makes the column sums of dK vanish
+    and dQ invariant to a shift of all keys; sum_j P_ij = 1 makes the column
+    sums of dV equal those of dO."""
+    r = _rng(20 + int(causal))
+    n, d, tau = 16, 8, 1 / math.sqrt(8)
+    q, k, v, dO = (2 * r.normal(size=(n, d)) for _ in range(4))
+    dq, dk, dvv, lse, D = oracle.attention_backward(q, k, v, dO, causal, tau)
+    o, lse_f = oracle.attention_forward(q, k, v, causal, tau)
+    assert np.max(np.abs(D - np.sum(dO * o, axis=1))) < 1e-12
+    assert np.max(np.abs(lse - lse_f)) < 1e-12
+    assert np.max(np.abs(dk.sum(axis=0))) < 1e-12
+    assert np.max(np.abs(dvv.sum(axis=0) - dO.sum(axis=0))) < 1e-12
+    w = r.normal(size=d)
+    dq2, _, _, _, _ = oracle.attention_backward(q, k + w, v, dO, causal, tau)
+    assert np.max(np.abs(dq2 - dq)) < 1e-11
+
+
+def test_backward_zero_upstream_gradient():
+    r = _rng(30)
+    q, k, v = r.normal(size=(7, 4)), r.normal(size=(7, 4)), r.normal(size=(7, 4))
+    dq, dk, dvv, _, D = oracle.attention_backward(q, k, v, np.zeros((7, 4)), True, 0.5)
+    assert not np.any(dq) and not np.any(dk) and not np.any(dvv) and not np.any(D)
+
+
+def test_backward_column_subset_matches_full():
+    r = _rng(31)
+    n = 12
+    q, k, v, dO = (r.normal(size=(n, 4)) for _ in range(4))
+    dq, dk, dvv, lse, D = oracle.attention_backward(q, k, v, dO, True, 0.5)
+    cols = [11, 2, 5]
+    dk2, dv2 = oracle.attention_backward_cols(q, k, v, dO, lse, D, True, 0.5, cols=cols)
+    assert np.array_equal(dk2, dk[cols]) and np.array_equal(dv2, dvv[cols])
+    lse3, D3, dq3 = oracle.attention_backward_rows(q, k, v, dO, True, 0.5, rows=[4, 9])
+    assert np.array_equal(dq3, dq[[4, 9]]) and np.array_equal(D3, D[[4, 9]])
