@@ -1,0 +1,125 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) exact IO-aware attention library.
+ *
+ * The library computes exact multi-head scaled-dot-product attention and its
+ * backward pass tile by tile, never writing an N x N score or probability
+ * matrix to device memory.  What is computed, per batch b and head h, with
+ * tau = `scale`:
+ *
+ *   S = tau Q K^T,  s_ij = -inf for j > i when `causal`,
+ *   P = row softmax(S),  O = P V,  lse_i = ln sum_j exp(s_ij)
+ *     (sj-techlog "FlashAttention 원 논문 해부", section "원 논문의 정의";
+ *      wonbeomjang.kr FlashAttention-2 review, "개선 2: m과 l 대신 L만 저장")
+ *
+ *   D_i = sum_k dO_ik O_ik,  dS_ij = P_ij (dP_ij - D_i),  dP = dO V^T,
+ *   dV = P^T dO,  dQ = tau dS K,  dK = tau dS^T Q
+ *     (FlashAttention-2 review, sections "Backward Pass"; the factor tau
+ *      comes from S = tau Q K^T).
+ *
+ * Conventions shared by every entry point
+ *  - Layout: Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays of
+ *    16-bit floats (bfloat16 for the plain names, IEEE half for the `_f16`
+ *    twins).  lse and D are contiguous [B, H, N] fp32.  dq_accum is a
+ *    contiguous [B, H, N, d] fp32 workspace.
+ *  - All pointers are DEVICE pointers of the current CUDA device and must be
+ *    16-byte aligned.  The caller allocates and owns every buffer; the library
+ *    allocates no device memory and keeps no per-call state.
+ *  - Sizes: B, H, N >= 1; d is 64 or 128; B*H <= 2^31-1; B*H*N*d < 2^62;
+ *    N <= 2^24.  scale must be finite and > 0 (callers usually pass
+ *    1/sqrt(d)).
+ *  - Causal masking is top-left aligned: key j is visible to query i iff
+ *    j <= i.  Every query row therefore sees at least key 0.
+ *  - Every call enqueues its kernels on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and returns without synchronising.  Argument
+ *    errors are detected on the host before anything is enqueued.  A launch
+ *    failure returns ATTN_ERR_LAUNCH.  Kernels never trap: a bounded wait that
+ *    runs out records ATTN_ERR_TIMEOUT in the library's device status word,
+ *    read with attn_get_device_status().
+ *  - Return value: an attn_status code (0 = success).  Nothing throws.
+ */
+#ifndef IO_AWARE_EXACT_GB300_ATTN_H
+#define IO_AWARE_EXACT_GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad scale */
+    ATTN_ERR_UNSUPPORTED_HEAD_DIM = 2, /* d not in {64, 128} */
+    ATTN_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned */
+    ATTN_ERR_UNSUPPORTED_DEVICE = 4,   /* current device is not sm_103 */
+    ATTN_ERR_LAUNCH = 5,               /* CUDA launch / driver error */
+    ATTN_ERR_TIMEOUT = 6,              /* a kernel's bounded wait ran out */
+    ATTN_ERR_DEVICE_FAULT = 7          /* CUDA reported an error while syncing */
+} attn_status;
+
+/*
+ * Forward pass.  Reads q, k, v [B,H,N,d]; writes o [B,H,N,d] and lse [B,H,N]
+ * (natural-log logsumexp of each row's scaled, masked scores).  The row
+ * statistics and output follow the FlashAttention-2 forward (FlashAttention-2
+ * review, "결과: FlashAttention-2 Forward 알고리즘"): online softmax over key
+ * blocks with one final division by the normaliser.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Backward pre-processing (FlashAttention-2 review, "Backward Pass" of
+ * FlashAttention-2: D_i = rowsum(dO_i o O_i) computed ahead of the main loop).
+ * Reads o and dO [B,H,N,d]; writes D [B,H,N] and sets dq_accum [B,H,N,d] to
+ * zero.  Must precede attn_bwd on the same stream.
+ */
+int attn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum,
+                        int B, int H, int N, int d, void* stream);
+int attn_bwd_preprocess_f16(const void* o, const void* dO, float* D, float* dq_accum,
+                            int B, int H, int N, int d, void* stream);
+
+/*
+ * Backward pass (recomputation of S and P from lse, sj-techlog page, section
+ * "forward가 끝난 뒤 backward는 무엇을 저장하고 무엇을 다시 계산하는가";
+ * K/V-block outer loop of the FlashAttention-2 backward).  Reads q, k, v, dO
+ * [B,H,N,d], lse and D [B,H,N] (from attn_fwd and attn_bwd_preprocess with the
+ * same arguments), accumulates into dq_accum (zeroed by the preprocess), and
+ * writes dq, dk, dv [B,H,N,d].  `o` is accepted for interface symmetry and may
+ * be NULL.  dq_accum is left holding tau^-1 dQ in fp32 (unspecified to
+ * callers).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, const float* D, float* dq_accum,
+             void* dq, void* dk, void* dv,
+             int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, const float* D, float* dq_accum,
+                 void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Static English description of a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel gave up a
+ * wait), or ATTN_ERR_DEVICE_FAULT (the synchronisation itself failed).
+ */
+int attn_get_device_status(void* stream);
+
+/*
+ * Self-test of the failure path: launches one tiny kernel that waits on a
+ * barrier nothing ever completes, with a wait limit of `timeout_us`
+ * microseconds (1..1000000).  The kernel records ATTN_ERR_TIMEOUT and
+ * returns; the GPU context stays usable.  Returns ATTN_OK once enqueued.
+ */
+int attn_selftest_timeout(int timeout_us, void* stream);
+
+/* Library version, for diagnostics. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IO_AWARE_EXACT_GB300_ATTN_H */

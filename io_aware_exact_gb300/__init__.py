@@ -1,1 +1,223 @@
-"""GB300-native exact IO-aware attention (placeholder; binding follows)."""
+"""GB300-native exact IO-aware attention.
+
+The compute lives in ``libattn_gb300.so`` (CUDA, sm_103a; C ABI declared in
+``include/attn.h``).  This package is a thin ctypes binding:
+
+* ``attn_fwd``, ``attn_bwd_preprocess``, ``attn_bwd`` (and ``*_f16``) take
+  raw device pointers (ints), sizes and a ``cudaStream_t`` (int) exactly like
+  the C functions, and raise :class:`AttnError` on a non-zero status;
+* ``forward`` / ``backward`` / :class:`AttnFunction` marshal PyTorch CUDA
+  tensors (which own all memory) into those calls.
+
+There is no CPU or PyTorch fallback: if the library is missing or the device
+is not an sm_103 GPU, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "attn.h")
+
+_lib = None
+_lock = threading.Lock()
+
+STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED_HEAD_DIM",
+    3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_UNSUPPORTED_DEVICE", 5: "ATTN_ERR_LAUNCH",
+    6: "ATTN_ERR_TIMEOUT", 7: "ATTN_ERR_DEVICE_FAULT",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%d: %s)" % (where, STATUS.get(status, "?"), status,
+                                                     status_string(status) if _lib else ""))
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libattn_gb300.so is missing: build it with "
+                                   "`python -m io_aware_exact_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            fwd = [P, P, P, P, P, I, I, I, I, I, F, P]
+            pre = [P, P, P, P, I, I, I, I, P]
+            bwd = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+            for name, at in (("attn_fwd", fwd), ("attn_fwd_f16", fwd),
+                             ("attn_bwd_preprocess", pre), ("attn_bwd_preprocess_f16", pre),
+                             ("attn_bwd", bwd), ("attn_bwd_f16", bwd)):
+                fn = getattr(L, name)
+                fn.argtypes = at
+                fn.restype = I
+            L.attn_status_string.argtypes = [I]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_get_device_status.argtypes = [P]
+            L.attn_get_device_status.restype = I
+            L.attn_selftest_timeout.argtypes = [I, P]
+            L.attn_selftest_timeout.restype = I
+            L.attn_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def header_functions():
+    """Names of the functions declared in include/attn.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(attn_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().attn_version().decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise AttnError(rc, where)
+
+
+# ---------------------------------------------------------------------------
+# Raw C-ABI calls (pointers as ints)
+# ---------------------------------------------------------------------------
+
+def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream, f16=False):
+    fn = lib().attn_fwd_f16 if f16 else lib().attn_fwd
+    _check(fn(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale), stream),
+           "attn_fwd")
+
+
+def attn_bwd_preprocess(o, dO, D, dq_accum, B, H, N, d, stream, f16=False):
+    fn = lib().attn_bwd_preprocess_f16 if f16 else lib().attn_bwd_preprocess
+    _check(fn(o, dO, D, dq_accum, B, H, N, d, stream), "attn_bwd_preprocess")
+
+
+def attn_bwd(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+             f16=False):
+    fn = lib().attn_bwd_f16 if f16 else lib().attn_bwd
+    _check(fn(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, int(bool(causal)),
+              float(scale), stream), "attn_bwd")
+
+
+def attn_get_device_status(stream=None) -> int:
+    return int(lib().attn_get_device_status(stream))
+
+
+def attn_selftest_timeout(timeout_us: int, stream=None):
+    _check(lib().attn_selftest_timeout(int(timeout_us), stream), "attn_selftest_timeout")
+
+
+# ---------------------------------------------------------------------------
+# PyTorch tensor marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_qkv(*ts):
+    torch = _torch()
+    t0 = ts[0]
+    if t0.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    if t0.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("expected bfloat16 or float16 tensors")
+    for t in ts:
+        if t.shape != t0.shape or t.dtype != t0.dtype:
+            raise ValueError("q, k, v (and o, dO) must share shape and dtype")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    return t0.shape, t0.dtype == torch.float16
+
+
+def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=None):
+    """O, lse for [B,H,N,d] CUDA tensors (outputs allocated by torch if not given)."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+             B, H, N, d, causal, scale, _stream_handle(stream), f16)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=None, dv=None,
+             D=None, dq_accum=None, stream=None):
+    """dQ, dK, dV for [B,H,N,d] CUDA tensors (workspace allocated by torch if not given)."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v, o, dO)
+    scale = d ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    D = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if D is None else D
+    if dq_accum is None:
+        dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    s = _stream_handle(stream)
+    attn_bwd_preprocess(o.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(),
+                        B, H, N, d, s, f16)
+    attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+             lse.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+             dv.data_ptr(), B, H, N, d, causal, scale, s, f16)
+    return dq, dk, dv
+
+
+def _autograd_function():
+    torch = _torch()
+
+    class AttnFunction(torch.autograd.Function):
+        """Exact attention with the library's forward and backward kernels.
+
+        Saves q, k, v, o and lse (O(N) extra per row, no N x N buffer) and
+        recomputes P in the backward, like the FlashAttention autograd
+        function described on the sj-techlog page ("1. Python interface는
+        scale·RNG state·작은 통계를 autograd에 넘긴다").
+        """
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal=False, scale=None):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            o, lse = forward(q, k, v, causal, scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.causal, ctx.scale = causal, scale
+            return o
+
+        @staticmethod
+        def backward(ctx, dO):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, o, lse, dO.contiguous(), ctx.causal, ctx.scale)
+            return dq, dk, dv, None, None
+
+    return AttnFunction
+
+
+def attention(q, k, v, causal: bool = False, scale=None):
+    """Differentiable exact attention over [B,H,N,d] bf16/fp16 CUDA tensors."""
+    global AttnFunction
+    if AttnFunction is None:
+        AttnFunction = _autograd_function()
+    return AttnFunction.apply(q, k, v, causal, scale)
+
+
+AttnFunction = None

@@ -1,0 +1,296 @@
+// attn_api.cu - C ABI entry points: argument checks, TMA tensor maps, launches.
+//
+// The host layer plays the part of the reference's C++ dispatcher (sj-techlog
+// "FlashAttention 원 논문 해부", section "3. C++ dispatcher는 N² buffer를 언제
+// 만들지 명시적으로 고른다": device/shape/head-size checks, then a launch on
+// the caller's stream) but allocates nothing: every buffer is the caller's.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_common.cuh"
+
+namespace attn {
+
+// Device status word written by kernels whose bounded waits run out.
+__device__ int g_status;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per CTA
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct DevInfo {
+    bool checked = false;
+    bool ok = false;
+    int* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Validates the current device (sm_103) and returns its status-word address.
+int current_device(int** status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return ATTN_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& di = g_dev[dev];
+    if (!di.checked) {
+        di.checked = true;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        void* p = nullptr;
+        di.ok = (major == 10 && minor == 3) &&
+                cudaGetSymbolAddress(&p, g_status) == cudaSuccess && p != nullptr;
+        di.status = static_cast<int*>(p);
+        if (!di.ok) cudaGetLastError();
+    }
+    if (!di.ok) return ATTN_ERR_UNSUPPORTED_DEVICE;
+    *status = di.status;
+    return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+    if (static_cast<long long>(B) * H > 2147483647LL) return ATTN_ERR_INVALID_ARG;
+    if (N > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+int check_scale(float s) { return (std::isfinite(s) && s > 0.f) ? ATTN_OK : ATTN_ERR_INVALID_ARG; }
+
+// 3-D tensor map over a contiguous [BH, N, d] 16-bit array: box = 64 columns x
+// 128 rows x 1 head, 128-byte swizzle, zero fill beyond row N of each head.
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return ATTN_ERR_LAUNCH;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kTile), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int map_launch(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, int causal, float scale, void* stream, bool bf16) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    int rc = check_shape(B, H, N, d);
+    if (rc) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BH, N, d, bf16)))
+        return rc;
+    FwdArgs a{};
+    a.o = o;
+    a.lse = lse;
+    a.status = status;
+    a.N = N;
+    a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
+    a.scale_log2 = scale * kLog2e;
+    a.timeout_ns = kDefaultTimeoutNs;
+    return map_launch(launch_fwd(tq, tk, tv, a, BH, d, causal != 0, bf16,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int pre_impl(const void* o, const void* dO, float* D, float* dq_accum, int B, int H, int N, int d,
+             void* stream, bool bf16) {
+    if (!o || !dO || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
+    int rc = check_shape(B, H, N, d);
+    if (rc) return rc;
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(D) || !aligned16(dq_accum))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    BwdPreArgs a{};
+    a.o = o;
+    a.dO = dO;
+    a.D = D;
+    a.dq_accum = dq_accum;
+    a.rows = static_cast<long long>(B) * H * N;
+    a.d = d;
+    return map_launch(launch_bwd_preprocess(a, bf16, static_cast<cudaStream_t>(stream)));
+}
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* /*o*/, const void* dO,
+             const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
+             int B, int H, int N, int d, int causal, float scale, void* stream, bool bf16) {
+    if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
+        return ATTN_ERR_INVALID_ARG;
+    int rc = check_shape(B, H, N, d);
+    if (rc) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+        !aligned16(D) || !aligned16(dq_accum) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BwdArgs a{};
+    a.lse = lse;
+    a.D = D;
+    a.dq_accum = dq_accum;
+    a.dk = dk;
+    a.dv = dv;
+    a.status = status;
+    a.N = N;
+    a.num_kvblocks = (N + kTile - 1) / kTile;
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.timeout_ns = kDefaultTimeoutNs;
+    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16, st))))
+        return rc;
+    DqConvertArgs c{};
+    c.dq_accum = dq_accum;
+    c.dq = dq;
+    c.elems = static_cast<long long>(BH) * N * d;
+    c.scale = scale;
+    return map_launch(launch_dq_convert(c, bf16, st));
+}
+
+__global__ void selftest_timeout_kernel(int* status, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on the barrier: the wait must run out and report.
+    const WaitCtx wc{&abort_flag, status, globaltimer_ns() + timeout_ns};
+    if (threadIdx.x == 0) (void)wait_bar(wc, b, 0);
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, int causal, float scale, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, stream, true);
+}
+
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, stream, false);
+}
+
+int attn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum, int B, int H,
+                        int N, int d, void* stream) {
+    return pre_impl(o, dO, D, dq_accum, B, H, N, d, stream, true);
+}
+
+int attn_bwd_preprocess_f16(const void* o, const void* dO, float* D, float* dq_accum, int B,
+                            int H, int N, int d, void* stream) {
+    return pre_impl(o, dO, D, dq_accum, B, H, N, d, stream, false);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
+             int B, int H, int N, int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale,
+                    stream, true);
+}
+
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale,
+                    stream, false);
+}
+
+const char* attn_status_string(int s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dimension (d must be 64 or 128)";
+        case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case ATTN_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+        case ATTN_ERR_LAUNCH: return "CUDA launch failed";
+        case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+        case ATTN_ERR_DEVICE_FAULT: return "CUDA reported an error while synchronising";
+        default: return "unknown status";
+    }
+}
+
+int attn_get_device_status(void* stream) {
+    int* status = nullptr;
+    int rc = current_device(&status);
+    if (rc) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_DEVICE_FAULT;
+    }
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_DEVICE_FAULT;
+    }
+    if (v == DEV_OK) return ATTN_OK;
+    return v == DEV_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_LAUNCH;
+}
+
+int attn_selftest_timeout(int timeout_us, void* stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return ATTN_ERR_INVALID_ARG;
+    int* status = nullptr;
+    int rc = current_device(&status);
+    if (rc) return rc;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        status, static_cast<unsigned long long>(timeout_us) * 1000ull);
+    return map_launch(cudaGetLastError());
+}
+
+const char* attn_version(void) { return "io_aware_exact_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,545 @@
+// attn_bwd.cu - exact attention backward for sm_103a (TMA + tcgen05 + TMEM).
+//
+// Three kernels, launched in this order on the caller's stream:
+//  1. preprocess: D_i = sum_k dO_ik O_ik (fp32) and dq_accum := 0
+//     (wonbeomjang.kr FlashAttention-2 review, "Backward Pass" of
+//     FlashAttention-2: D is computed ahead of the main loop);
+//  2. main kernel, K/V-block outer loop (same review: each CTA owns dK_j, dV_j
+//     and needs no inter-CTA synchronisation; dQ is accumulated across CTAs
+//     with atomic adds).  Per (b, h, 128-key block j), for each 128-query
+//     block i that can see block j:
+//        S^T  = K_j Q_i^T              (recomputed; sj-techlog "FlashAttention
+//        dP^T = V_j dO_i^T              원 논문 해부", backward section)
+//        P^T  = exp(tau S^T - lse_i)   (FlashAttention-2 review, "개선 2")
+//        dS^T = P^T o (dP^T - D_i)     (review, "Backward Pass": softmax grad)
+//        dQ_i += dS_ij K_j   (fp32 atomics into dq_accum)
+//        dV_j += P^T dO_i,   dK_j += dS^T Q_i
+//     and finally dK_j *= tau (S = tau Q K^T);
+//  3. convert: dQ = tau * dq_accum, rounded to the 16-bit type.
+//
+// GB300 mapping of the main kernel (our design):
+//  * TMEM (512 columns): S^T at 0, dP^T at 128, dV at 256, dK at 256 + d.
+//    P^T (16-bit pairs) overwrites S^T columns [0,64) and dS^T overwrites
+//    dP^T columns [128,192); both feed the dV / dK MMAs straight from TMEM.
+//    dQ_i = dS K_j lands in the freed columns [64,128) (d columns 0..63) and
+//    [192,256) (d columns 64..127), is read out and atomically added.
+//  * dS^T is also written to shared memory (128-byte swizzle) as the
+//    MN-major A operand of the dQ MMA.
+//  * warp 0: TMA (K_j, V_j once; Q_i, dO_i through a ring), warp 1: MMA
+//    issuer, warp 2: TMEM owner, warp 3: loads lse_i, D_i into shared memory,
+//    warps 4-11: two compute warpgroups, each one key per thread (TMEM lane)
+//    and half of the 128 query columns.
+#include "attn_common.cuh"
+
+namespace attn {
+
+// ============================================================================
+// 1. preprocess
+// ============================================================================
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256)
+attn_bwd_preprocess_kernel(const BwdPreArgs a) {
+    constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const int sub = threadIdx.x % TPR;
+    const long long rows_per_sweep = nthreads / TPR;
+    const long long sweeps = (a.rows + rows_per_sweep - 1) / rows_per_sweep;
+    // every thread runs the same number of sweeps, so the row-group shuffles
+    // below always see all 32 lanes of the warp
+    for (long long sw = 0; sw < sweeps; ++sw) {
+        const long long row = sw * rows_per_sweep + tid / TPR;
+        const bool valid = row < a.rows;
+        float acc = 0.f;
+        if (valid) {
+            const uint4 o4 = reinterpret_cast<const uint4*>(a.o)[row * TPR + sub];
+            const uint4 d4 = reinterpret_cast<const uint4*>(a.dO)[row * TPR + sub];
+            const uint16_t* oh = reinterpret_cast<const uint16_t*>(&o4);
+            const uint16_t* dh = reinterpret_cast<const uint16_t*>(&d4);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(to_f32<BF16>(oh[e]), to_f32<BF16>(dh[e]), acc);
+            float4* z = reinterpret_cast<float4*>(a.dq_accum + row * D + sub * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+        if (valid && sub == 0) a.D[row] = acc;
+    }
+}
+
+// ============================================================================
+// 3. dQ convert
+// ============================================================================
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_dq_convert_kernel(const DqConvertArgs a) {
+    const long long n8 = a.elems / 8;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += stride) {
+        const float4 x = reinterpret_cast<const float4*>(a.dq_accum)[2 * i];
+        const float4 y = reinterpret_cast<const float4*>(a.dq_accum)[2 * i + 1];
+        uint4 r;
+        r.x = pack2<BF16>(x.x * a.scale, x.y * a.scale);
+        r.y = pack2<BF16>(x.z * a.scale, x.w * a.scale);
+        r.z = pack2<BF16>(y.x * a.scale, y.y * a.scale);
+        r.w = pack2<BF16>(y.z * a.scale, y.w * a.scale);
+        reinterpret_cast<uint4*>(a.dq)[i] = r;
+    }
+}
+
+// ============================================================================
+// 2. main backward kernel
+// ============================================================================
+template <int D>
+struct BwdCfg {
+    static constexpr int STAGES = (D == 128) ? 2 : 3;       // Q_i / dO_i ring depth
+    static constexpr int KBOX = D / kBoxCols;
+    static constexpr int TILE_BYTES = kTile * D * 2;        // 128 x D 16-bit tile
+    static constexpr int DS_BYTES = kTile * kTile * 2;      // dS^T, 128 keys x 128 queries
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + TILE_BYTES;
+    static constexpr int DS_OFF = V_OFF + TILE_BYTES;
+    static constexpr int Q_OFF = DS_OFF + DS_BYTES;
+    static constexpr int DO_OFF = Q_OFF + STAGES * TILE_BYTES;
+    static constexpr int STAT_OFF = DO_OFF + STAGES * TILE_BYTES;   // lse2[S][128], Dv[S][128]
+    static constexpr int BAR_OFF = STAT_OFF + STAGES * 2 * kTile * 4;
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_QFULL = 1;
+    static constexpr int B_DOFULL = B_QFULL + STAGES;
+    static constexpr int B_QEMPTY = B_DOFULL + STAGES;
+    static constexpr int B_STFULL = B_QEMPTY + STAGES;      // stats ready  [S]
+    static constexpr int B_STEMPTY = B_STFULL + STAGES;     // stats free   [S]
+    static constexpr int B_SDP = B_STEMPTY + STAGES;        // S^T and dP^T in TMEM
+    static constexpr int B_DS = B_SDP + 1;                  // P^T, dS^T written
+    static constexpr int B_DQFULL = B_DS + 1;               // dQ in TMEM
+    static constexpr int B_DQEMPTY = B_DQFULL + 1;          // dQ read out
+    static constexpr int B_ACC = B_DQEMPTY + 1;             // dV, dK final
+    static constexpr int B_LDDONE = B_ACC + 1;             // both warpgroups read S^T/dP^T
+    static constexpr int B_DRAIN = B_LDDONE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    // The d=128 layout needs (almost) all 227 KB, so it relies on the dynamic
+    // shared-memory window starting 1024-byte aligned (checked at run time).
+    static constexpr int SLACK = (D == 128) ? 0 : 1024;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + SLACK;
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+    __device__ static constexpr uint32_t dq_col(int h) { return h == 0 ? 64u : 192u; }
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdArgs args) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    if (pad > static_cast<uint32_t>(C::SLACK)) {
+        // the layout does not fit this placement; report instead of faulting
+        if (threadIdx.x == 0) atomicExch(args.status, DEV_SMEM_ALIGN);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+    float* stats = reinterpret_cast<float*>(smem + C::STAT_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int j = blockIdx.y;                    // key block (causal: small j = most work)
+    const int N = args.N;
+    const int nq = args.num_kvblocks;            // query blocks == key blocks
+    const int i_start = CAUSAL ? j : 0;
+    const int n_it = nq - i_start;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_KVFULL), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar(C::B_QFULL + s), 1);
+            mbar_init(bar(C::B_DOFULL + s), 1);
+            mbar_init(bar(C::B_QEMPTY + s), 1);
+            mbar_init(bar(C::B_STFULL + s), 32);
+            mbar_init(bar(C::B_STEMPTY + s), 256);
+        }
+        mbar_init(bar(C::B_SDP), 1);
+        mbar_init(bar(C::B_DS), 256);
+        mbar_init(bar(C::B_DQFULL), 1);
+        mbar_init(bar(C::B_DQEMPTY), 256);
+        mbar_init(bar(C::B_ACC), 1);
+        mbar_init(bar(C::B_LDDONE), 256);
+        mbar_init(bar(C::B_DRAIN), 1);
+        // A failure recorded earlier on this device turns later CTAs into
+        // no-ops until the host reads and clears the status word.
+        *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const bool skip = *abort_flag != 0;
+
+    if (skip) {
+        // nothing issued, nothing to drain
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_kv = policy_evict_first();
+            const uint64_t pol_q = policy_evict_last();
+            mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
+            for (int b = 0; b < C::KBOX; ++b) {
+                tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
+                            j * kTile, bh, pol_kv);
+                tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
+                            j * kTile, bh, pol_kv);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::STAGES;
+                const int i = i_start + it;
+                if (it >= C::STAGES) {
+                    ok = wait_bar(wc, bar(C::B_QEMPTY + s), ((it / C::STAGES) - 1) & 1);
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                bar(C::B_QFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
+                mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
+                                bar(C::B_DOFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
+                issued = it + 1;
+            }
+            if (!ok) {
+                drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
+                for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+                    const int s = it % C::STAGES;
+                    drain_wait(bar(C::B_QFULL + s), (it / C::STAGES) & 1, 1000000000ull);
+                    drain_wait(bar(C::B_DOFULL + s), (it / C::STAGES) & 1, 1000000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = BF16 ? 1u : 0u;
+            constexpr uint32_t id_kk = idesc_f16(128, 128, fmt, 0, 0);  // K x Q^T, V x dO^T
+            constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
+            constexpr uint32_t id_dq = idesc_f16(128, 64, fmt, 1, 1);   // dS x K (both MN-major)
+            bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
+                if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
+                tc_fence_after();
+                const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
+                const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
+                // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::S_COL,
+                           smem_desc(sbase + C::K_OFF + off, 16, 1024, LAYOUT_SW128),
+                           smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                }
+                if (!(ok = wait_bar(wc, bar(C::B_DOFULL + s), ph))) break;
+                tc_fence_after();
+                // dP^T = V dO^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::DP_COL,
+                           smem_desc(sbase + C::V_OFF + off, 16, 1024, LAYOUT_SW128),
+                           smem_desc(do_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                }
+                mma_commit(bar(C::B_SDP));
+                if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
+                tc_fence_after();
+                // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss(tmem + C::dq_col(h),
+                               smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                               smem_desc(sbase + C::K_OFF + h * kBoxBytes + kk * 2048, kBoxBytes, 1024,
+                                         LAYOUT_SW128),
+                               id_dq, kk > 0);
+                }
+                mma_commit(bar(C::B_DQFULL));
+                // dV += P^T dO ; dK += dS^T Q
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8,
+                           smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8,
+                           smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(C::B_QEMPTY + s));
+            }
+            if (ok) mma_commit(bar(C::B_ACC));
+            mma_commit(bar(C::B_DRAIN));
+            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ lse / D loader
+        const float* lse_g = args.lse + static_cast<size_t>(bh) * N;
+        const float* d_g = args.D + static_cast<size_t>(bh) * N;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % C::STAGES;
+            if (it >= C::STAGES &&
+                !__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_STEMPTY + s), ((it / C::STAGES) - 1) & 1)))
+                break;
+            const int q0 = (i_start + it) * kTile;
+            float* l2 = stats + s * 2 * kTile;
+            float* dv = l2 + kTile;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int qi = q0 + lane * 4 + e;
+                const bool valid = qi < N;
+                // P = exp(tau s - lse) = exp2(tau log2e s - lse log2e); rows past N get P = 0
+                l2[lane * 4 + e] = valid ? lse_g[qi] * kLog2e : INFINITY;
+                dv[lane * 4 + e] = valid ? d_g[qi] : 0.f;
+            }
+            mbar_arrive(bar(C::B_STFULL + s));
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ compute warpgroups
+        const int c = (warp - 4) >> 2;           // query half handled by this warpgroup
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;            // TMEM lane: key row (and query row for dQ)
+        const int key = j * kTile + r;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const float cs = args.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % C::STAGES;
+            const int i = i_start + it;
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SDP), it & 1) &&
+                                             wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tmem + lane_off + C::S_COL + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(tmem + lane_off + C::S_COL + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+            tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+            tmem_ld_wait();
+            // both warpgroups have read their S^T / dP^T columns before either
+            // overwrites them (bounded wait instead of a named barrier)
+            mbar_arrive(bar(C::B_LDDONE));
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LDDONE), it & 1));
+            if (!ok) break;
+            const float* l2 = stats + s * 2 * kTile + 64 * c;
+            const float* dv = l2 + kTile;
+            const int qbase = i * kTile + 64 * c;
+            const bool key_ok = key < N;
+            const bool diag = CAUSAL && (i == j);
+            uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pp[16], pd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = 32 * h + 2 * e + u;
+                        float p = ex2_approx(fmaf(__uint_as_float(sr[q]), cs, -l2[q]));
+                        if (!key_ok || (diag && qbase + q < key)) p = 0.f;
+                        pv[u] = p;
+                        dsv[u] = p * (__uint_as_float(dr[q]) - dv[q]);
+                    }
+                    pp[e] = pack2<BF16>(pv[0], pv[1]);
+                    pd[e] = pack2<BF16>(dsv[0], dsv[1]);
+                }
+                tmem_st16(tmem + lane_off + C::S_COL + 32 * c + 16 * h, pp);
+                tmem_st16(tmem + lane_off + C::DP_COL + 32 * c + 16 * h, pd);
+                // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of
+                // row r sits at chunk position k ^ (r % 8)
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int chunk = 4 * h + k4;
+                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
+                        make_uint4(pd[4 * k4], pd[4 * k4 + 1], pd[4 * k4 + 2], pd[4 * k4 + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_DS));
+            mbar_arrive(bar(C::B_STEMPTY + s));
+            // dQ_i readout: lane = query row of block i
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const int qrow = i * kTile + r;
+            float* dq_row = args.dq_accum + (static_cast<size_t>(bh) * N + qrow) * D;
+            if constexpr (D == 128) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t q32[32];
+                    tmem_ld32(tmem + lane_off + C::dq_col(c) + 32 * h, q32);
+                    tmem_ld_wait();
+                    if (qrow < N) {
+                        float4* dst = reinterpret_cast<float4*>(dq_row + 64 * c + 32 * h);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
+                                                            __uint_as_float(q32[4 * v4 + 1]),
+                                                            __uint_as_float(q32[4 * v4 + 2]),
+                                                            __uint_as_float(q32[4 * v4 + 3])));
+                    }
+                }
+            } else {
+                uint32_t q32[32];
+                tmem_ld32(tmem + lane_off + C::dq_col(0) + 32 * c, q32);
+                tmem_ld_wait();
+                if (qrow < N) {
+                    float4* dst = reinterpret_cast<float4*>(dq_row + 32 * c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
+                                                        __uint_as_float(q32[4 * v4 + 1]),
+                                                        __uint_as_float(q32[4 * v4 + 2]),
+                                                        __uint_as_float(q32[4 * v4 + 3])));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::B_DQEMPTY));
+        }
+        // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
+        if (ok) {
+            tc_fence_after();
+            const float mul = (c == 0) ? 1.0f : args.scale;
+            const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
+            uint16_t* out = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
+                            (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t a32[32];
+                tmem_ld32(tmem + lane_off + col + cc, a32);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack2<BF16>(__uint_as_float(a32[2 * e]) * mul,
+                                        __uint_as_float(a32[2 * e + 1]) * mul);
+                if (key < N) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + cc);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ============================================================================
+// launchers
+// ============================================================================
+static int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 152;
+    }
+    return n;
+}
+
+cudaError_t launch_bwd_preprocess(const BwdPreArgs& a, bool bf16, cudaStream_t stream) {
+    const long long rows_per_block = 256 / (a.d / 8);
+    long long blocks = (a.rows + rows_per_block - 1) / rows_per_block;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (a.d == 64) {
+        if (bf16) attn_bwd_preprocess_kernel<true, 64><<<blocks, 256, 0, stream>>>(a);
+        else attn_bwd_preprocess_kernel<false, 64><<<blocks, 256, 0, stream>>>(a);
+    } else if (a.d == 128) {
+        if (bf16) attn_bwd_preprocess_kernel<true, 128><<<blocks, 256, 0, stream>>>(a);
+        else attn_bwd_preprocess_kernel<false, 128><<<blocks, 256, 0, stream>>>(a);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream) {
+    long long blocks = (a.elems / 8 + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (bf16) attn_dq_convert_kernel<true><<<blocks, 256, 0, stream>>>(a);
+    else attn_dq_convert_kernel<false><<<blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool BF16>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdArgs& a, int BH,
+                                cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(BH, a.num_kvblocks);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int BH, int d, bool causal,
+                       bool bf16, cudaStream_t stream) {
+#define ATTN_BWD_CASE(D_, C_, B_) \
+    if (d == D_ && causal == C_ && bf16 == B_) return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, a, BH, stream);
+    ATTN_BWD_CASE(64, false, true)
+    ATTN_BWD_CASE(64, true, true)
+    ATTN_BWD_CASE(128, false, true)
+    ATTN_BWD_CASE(128, true, true)
+    ATTN_BWD_CASE(64, false, false)
+    ATTN_BWD_CASE(64, true, false)
+    ATTN_BWD_CASE(128, false, false)
+    ATTN_BWD_CASE(128, true, false)
+#undef ATTN_BWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

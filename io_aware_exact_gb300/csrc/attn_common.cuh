@@ -1,0 +1,77 @@
+// attn_common.cuh - shared declarations of the CUDA attention library.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Tile geometry shared by forward and backward: 128 query rows x 128 keys per
+// MMA tile; tiles are stored in shared memory as 64-column (128-byte) boxes
+// with the 128-byte swizzle, which is the layout the TMA box writes and the
+// tensor-core descriptors read.
+constexpr int kTile = 128;
+constexpr int kBoxCols = 64;
+constexpr int kBoxBytes = kTile * kBoxCols * 2;  // 16 KB
+
+struct FwdArgs {
+    void* o;               // [B*H, N, d] 16-bit, written
+    float* lse;            // [B*H, N] fp32, written (natural log, scale inside)
+    int* status;           // device status word
+    int N;                 // sequence length
+    int num_qblocks;       // ceil(N / 256): CTAs per head
+    float scale_log2;      // softmax scale * log2(e)
+    unsigned long long timeout_ns;
+};
+
+struct BwdPreArgs {
+    const void* o;         // [B*H, N, d]
+    const void* dO;        // [B*H, N, d]
+    float* D;              // [B*H, N]
+    float* dq_accum;       // [B*H, N, d] fp32, zeroed
+    long long rows;        // B*H*N
+    int d;
+};
+
+struct BwdArgs {
+    const float* lse;      // [B*H, N]
+    const float* D;        // [B*H, N]
+    float* dq_accum;       // [B*H, N, d] fp32 (accumulated with reductions)
+    void* dk;              // [B*H, N, d] 16-bit
+    void* dv;              // [B*H, N, d] 16-bit
+    int* status;
+    int N;
+    int num_kvblocks;      // ceil(N / 128)
+    float scale;           // softmax scale (tau)
+    float scale_log2;      // tau * log2(e)
+    unsigned long long timeout_ns;
+};
+
+struct DqConvertArgs {
+    const float* dq_accum;  // [B*H, N, d]
+    void* dq;               // [B*H, N, d] 16-bit
+    long long elems;        // B*H*N*d
+    float scale;            // tau
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, int BH, int d, bool causal, bool bf16,
+                       cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const BwdPreArgs& a, bool bf16, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int BH, int d, bool causal,
+                       bool bf16, cudaStream_t stream);
+cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+}
+
+}  // namespace attn

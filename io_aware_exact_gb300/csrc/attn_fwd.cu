@@ -1,0 +1,383 @@
+// attn_fwd.cu - exact attention forward for sm_103a (TMA + tcgen05 + TMEM).
+//
+// Computes, per (batch, head), O = softmax(tau Q K^T [+ causal mask]) V and
+// lse_i = ln sum_j exp(tau q_i.k_j) without writing any N x N matrix.
+//
+// Algorithm: the FlashAttention-2 forward (wonbeomjang.kr FlashAttention-2
+// review, "결과: FlashAttention-2 Forward 알고리즘"): Q-block outer loop
+// parallel over CTAs, K/V-block inner loop, running row max m and normaliser l,
+// unnormalised accumulator rescaled by exp(m_old - m_new), one division by l at
+// the end ("개선 1"), and the logsumexp L = m + log l stored for the backward
+// ("개선 2").  The merge rule is the one of sj-techlog "FlashAttention 원 논문
+// 해부", section "두 tile을 한 row로 합치는 식".  Fully masked causal tiles are
+// skipped ("Causal Masking 최적화" in the FlashAttention-2 review).
+//
+// GB300 mapping (our design, not the pages'):
+//  * one CTA = one (b, h) and 256 query rows, as two 128-row tiles that
+//    ping-pong on the tensor core: while the softmax warpgroup of one tile
+//    works, the MMAs of the other tile run;
+//  * warp 0 issues TMA loads (Q once, K/V through a multi-stage ring), warp 1
+//    issues tcgen05.mma from one thread, warp 2 owns the TMEM allocation,
+//    warps 4-7 and 8-11 are the softmax warpgroups of tile 0 and tile 1 (one
+//    thread per query row, since TMEM lane = row);
+//  * S = Q K^T lands in TMEM (fp32, 128 columns per tile); the softmax writes
+//    P as packed 16-bit pairs over the first 64 columns of the same region and
+//    the PV MMA reads P straight from TMEM; O accumulates in TMEM;
+//  * exponentials are exp2 with tau*log2(e) folded into one FMA; the running
+//    reference max is only moved when the row max grows by more than 2^8
+//    (exact: O and l always share the same reference, so the final O/l and
+//    lse are unchanged; it only bounds P by 256);
+//  * every wait is bounded; a timeout sets the device status word and the CTA
+//    drains its in-flight copies and MMAs, frees TMEM and exits.
+#include "attn_common.cuh"
+
+namespace attn {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int TILES = 2;                       // 128-row Q tiles per CTA
+    static constexpr int STAGES = (D == 128) ? 2 : 4;     // K/V ring depth
+    static constexpr int KBOX = D / kBoxCols;             // 64-column boxes per row
+    static constexpr int TILE_BYTES = kTile * D * 2;      // one 128 x D tile
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + TILES * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+    // barrier slots
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_VFULL = B_KFULL + STAGES;
+    static constexpr int B_KVEMPTY = B_VFULL + STAGES;
+    static constexpr int B_SFULL = B_KVEMPTY + STAGES;    // [2]
+    static constexpr int B_PFULL = B_SFULL + 2;           // [2]
+    static constexpr int B_OFULL = B_PFULL + 2;           // [2]
+    static constexpr int B_DRAIN = B_OFULL + 2;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + runtime alignment slack
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    // TMEM columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
+    __device__ static constexpr uint32_t s_col(int t) { return 128u * t; }
+    __device__ static constexpr uint32_t o_col(int t) { return 256u + D * t; }
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int qb = args.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // heavy blocks first
+    const int q0 = qb * (C::TILES * kTile);
+    const int N = args.N;
+    const int nkv_all = (N + kTile - 1) / kTile;
+    int nkv[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r0 = q0 + kTile * t;
+        nkv[t] = (r0 >= N) ? 0 : (CAUSAL ? min(nkv_all, r0 / kTile + 1) : nkv_all);
+    }
+    const int n_iter = max(nkv[0], nkv[1]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::B_SFULL + t), 1);
+            mbar_init(bar(C::B_PFULL + t), 128);
+            mbar_init(bar(C::B_OFULL + t), 1);
+        }
+        mbar_init(bar(C::B_DRAIN), 1);
+        // A failure recorded earlier on this device turns later CTAs into
+        // no-ops until the host reads and clears the status word.
+        *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const bool skip = *abort_flag != 0;
+
+    if (skip) {
+        // nothing issued, nothing to drain
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            const int ntiles = (nkv[1] > 0) ? 2 : 1;
+            mbar_arrive_expect_tx(bar(C::B_QFULL), ntiles * C::TILE_BYTES);
+            for (int t = 0; t < ntiles; ++t)
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::Q_OFF + t * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                bar(C::B_QFULL), b * kBoxCols, q0 + kTile * t, bh, pol_q);
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n_iter; ++j) {
+                const int s = j % C::STAGES;
+                if (j >= C::STAGES) {
+                    ok = wait_bar(wc, bar(C::B_KVEMPTY + s), ((j / C::STAGES) - 1) & 1);
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
+                                bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
+                                bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                issued = j + 1;
+            }
+            if (!ok) {
+                // let copies already in flight land before the CTA's smem goes away
+                drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
+                for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+                    drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                    drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = BF16 ? 1u : 0u;
+            constexpr uint32_t idesc_s = idesc_f16(128, 128, fmt, 0, 0);  // Q (K-major) x K (K-major)
+            constexpr uint32_t idesc_o = idesc_f16(128, D, fmt, 0, 1);    // P (TMEM) x V (MN-major)
+            auto issue_s = [&](int t, int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    const uint64_t a = smem_desc(sbase + C::Q_OFF + t * C::TILE_BYTES + off, 16,
+                                                 1024, LAYOUT_SW128);
+                    const uint64_t b = smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES + off, 16,
+                                                 1024, LAYOUT_SW128);
+                    mma_ss(tmem + C::s_col(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t b = smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES + kk * 2048,
+                                                 kBoxBytes, 1024, LAYOUT_SW128);
+                    mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, b, idesc_o,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait_bar(wc, bar(C::B_QFULL), 0) && wait_bar(wc, bar(C::B_KFULL + 0), 0);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (nkv[t] > 0) {
+                        issue_s(t, 0);
+                        mma_commit(bar(C::B_SFULL + t));
+                    }
+            }
+            for (int j = 0; ok && j < n_iter; ++j) {
+                const int s = j % C::STAGES;
+                if (!(ok = wait_bar(wc, bar(C::B_VFULL + s), (j / C::STAGES) & 1))) break;
+                bool next_k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nkv[t]) continue;
+                    if (!(ok = wait_bar(wc, bar(C::B_PFULL + t), j & 1))) break;
+                    tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    if (j + 1 < nkv[t]) {
+                        if (!next_k_ready) {
+                            const int s1 = (j + 1) % C::STAGES;
+                            if (!(ok = wait_bar(wc, bar(C::B_KFULL + s1), ((j + 1) / C::STAGES) & 1)))
+                                break;
+                            tc_fence_after();
+                            next_k_ready = true;
+                        }
+                        issue_s(t, (j + 1) % C::STAGES);
+                        mma_commit(bar(C::B_SFULL + t));
+                    } else {
+                        mma_commit(bar(C::B_OFULL + t));
+                    }
+                }
+                mma_commit(bar(C::B_KVEMPTY + s));
+            }
+            // make sure no MMA is still reading smem / writing TMEM at teardown
+            mma_commit(bar(C::B_DRAIN));
+            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;
+        const int wq = warp & 3;                 // TMEM lane quarter of this warp
+        const int r = wq * 32 + lane;            // row within the tile
+        const int row = q0 + kTile * t + r;      // row within the head
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + C::s_col(t);
+        const uint32_t o_addr = tmem + lane_off + C::o_col(t);
+        const float cs = args.scale_log2;
+        float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv[t]; ++j) {
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+            tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            tmem_ld_wait();
+            float* sv = reinterpret_cast<float*>(sr);
+            // mask: key tail (keys >= N) and, on the diagonal block, keys > row
+            int limit = N - j * kTile;
+            if (CAUSAL) limit = min(limit, row - j * kTile + 1);
+            if (limit < kTile) {
+#pragma unroll
+                for (int c = 0; c < kTile; ++c)
+                    if (c >= limit) sv[c] = -INFINITY;
+            }
+            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+            for (int c = 4; c < kTile; c += 4) {
+                mx0 = fmaxf(mx0, sv[c]);
+                mx1 = fmaxf(mx1, sv[c + 1]);
+                mx2 = fmaxf(mx2, sv[c + 2]);
+                mx3 = fmaxf(mx3, sv[c + 3]);
+            }
+            const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs);
+            const bool move = m_new > m_ref + 8.0f;
+            float alpha = 1.0f;
+            if (move) {
+                alpha = ex2_approx(m_ref - m_new);  // 0 on the first block
+                l *= alpha;
+                m_ref = m_new;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // O holds P V up to block j-1 (S of block j was committed after it)
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(o_addr + c, orr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                    tmem_st32(o_addr + c, orr);
+                }
+            }
+            const float nm = -m_ref;
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(sv[64 * h + 2 * e], cs, nm));
+                    const float p1 = ex2_approx(fmaf(sv[64 * h + 2 * e + 1], cs, nm));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[e] = pack2<BF16>(p0, p1);
+                }
+                tmem_st32(s_addr + 32 * h, pk);
+            }
+            l += sum0 + sum1;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL + t));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
+        if (ok && nkv[t] > 0) {
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+            const bool valid = row < N;
+            using Vec = uint4;
+            Vec* dst = reinterpret_cast<Vec*>(static_cast<uint16_t*>(args.o) +
+                                              (static_cast<size_t>(bh) * N + row) * D);
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t orr[32];
+                tmem_ld32(o_addr + c, orr);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                        __uint_as_float(orr[2 * e + 1]) * inv_l);
+                if (valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[c / 8 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                     pk[4 * v4 + 3]);
+                }
+            }
+            if (valid)
+                args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const FwdArgs& a, int BH,
+                                cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = attn_fwd_kernel<D, CAUSAL, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(BH, a.num_qblocks);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, int BH, int d, bool causal, bool bf16,
+                       cudaStream_t stream) {
+#define ATTN_FWD_CASE(D_, C_, B_) \
+    if (d == D_ && causal == C_ && bf16 == B_) return launch_fwd_t<D_, C_, B_>(tq, tk, tv, a, BH, stream);
+    ATTN_FWD_CASE(64, false, true)
+    ATTN_FWD_CASE(64, true, true)
+    ATTN_FWD_CASE(128, false, true)
+    ATTN_FWD_CASE(128, true, true)
+    ATTN_FWD_CASE(64, false, false)
+    ATTN_FWD_CASE(64, true, false)
+    ATTN_FWD_CASE(128, false, false)
+    ATTN_FWD_CASE(128, true, false)
+#undef ATTN_FWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -115,8 +115,12 @@ def attention_forward(q, k, v, causal: bool, scale: float, rows=None):
     return o, lse
 
 
-def attention_backward_rows(q, k, v, dO, causal: bool, scale: float, rows=None):
-    """(lse, D, dQ) of one head for the selected query rows (all by default)."""
+def attention_backward_rows(q, k, v, dO, causal: bool, scale: float, rows=None,
+                            with_dq: bool = True):
+    """(lse, D, dQ) of one head for the selected query rows (all by default).
+
+    With ``with_dq=False`` only lse and D are computed and dQ is None.
+    """
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     nq, d = q.shape
     nk, dv = v.shape
@@ -124,10 +128,11 @@ def attention_backward_rows(q, k, v, dO, causal: bool, scale: float, rows=None):
     r = _idx(rows, nq)
     lse = np.empty((r.size,), np.float64)
     D = np.empty((r.size,), np.float64)
-    dq = np.empty((r.size, d), np.float64)
+    dq = np.empty((r.size, d), np.float64) if with_dq else None
+    dq_p = _p(dq) if with_dq else ctypes.POINTER(ctypes.c_double)()
     rc = _load().oracle_attn_bwd_rows(_p(q), _p(k), _p(v), _p(dO), nq, nk, d, dv,
                                       int(bool(causal)), float(scale), _p(r), r.size,
-                                      _p(lse), _p(D), _p(dq))
+                                      _p(lse), _p(D), dq_p)
     if rc != 0:
         raise ValueError("oracle_attn_bwd_rows rejected its arguments")
     return lse, D, dq

@@ -116,7 +116,7 @@ int oracle_attn_fwd_rows(const double* q, const double* k, const double* v,
 /*
  * Backward, row pass, for the listed query rows:
  *   lse_out[r] = lse_i,   D_out[r] = sum_j P_ij dP_ij,
- *   dq_out[r][d] = tau * sum_j dS_ij k_j.
+ *   dq_out[r][d] = tau * sum_j dS_ij k_j   (skipped when dq_out is NULL).
  */
 int oracle_attn_bwd_rows(const double* q, const double* k, const double* v,
                          const double* dO,
@@ -150,12 +150,14 @@ int oracle_attn_bwd_rows(const double* q, const double* k, const double* v,
                 dp[j] = dot(doi, v + j * dv, dv);       /* dP_ij = dO_i . v_j */
                 D += s[j] * dp[j];
             }
-            double* dqi = dq_out + r * d;
-            for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
-            for (int64_t j = 0; j < nvis; ++j) {
-                const double ds = s[j] * (dp[j] - D);  /* dS_ij */
-                const double* kj = k + j * d;
-                for (int64_t c = 0; c < d; ++c) dqi[c] += tau * ds * kj[c];
+            if (dq_out) {
+                double* dqi = dq_out + r * d;
+                for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
+                for (int64_t j = 0; j < nvis; ++j) {
+                    const double ds = s[j] * (dp[j] - D);  /* dS_ij */
+                    const double* kj = k + j * d;
+                    for (int64_t c = 0; c < d; ++c) dqi[c] += tau * ds * kj[c];
+                }
             }
             lse_out[r] = lse;
             D_out[r] = D;

@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The library is built with nvcc (cross-compiling for sm_103a) and loaded with
+ctypes; these tests check that it exports every function include/attn.h
+declares and that argument errors are reported synchronously with the
+documented codes, before any device work.
+"""
+import ast
+import re
+import glob
+import os
+
+import pytest
+
+import io_aware_exact_gb300 as attn
+from io_aware_exact_gb300 import build as attn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    attn_build.build()
+    return attn.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = attn.header_functions()
+    assert {"attn_fwd", "attn_bwd_preprocess", "attn_bwd"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert attn.status_string(code)
+    assert "aligned" in attn.status_string(3)
+    assert attn.version().startswith("io_aware_exact_gb300")
+
+
+A = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these tests
+
+
+def _fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return L.attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def _bwd(L, **kw):
+    a = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, D=A, acc=A, dq=A, dk=A, dv=A, B=1, H=1, N=128,
+             d=64, causal=0, scale=0.125)
+    a.update(kw)
+    return L.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["D"], a["acc"],
+                      a["dq"], a["dk"], a["dv"], a["B"], a["H"], a["N"], a["d"], a["causal"],
+                      a["scale"], None)
+
+
+def test_forward_argument_errors(L):
+    assert _fwd(L, q=None) == 1
+    assert _fwd(L, lse=None) == 1
+    assert _fwd(L, B=0) == 1
+    assert _fwd(L, N=0) == 1
+    assert _fwd(L, N=(1 << 24) + 1) == 1
+    assert _fwd(L, d=32) == 2
+    assert _fwd(L, d=96) == 2
+    assert _fwd(L, d=256) == 2
+    assert _fwd(L, scale=0.0) == 1
+    assert _fwd(L, scale=-1.0) == 1
+    assert _fwd(L, scale=float("nan")) == 1
+    assert _fwd(L, scale=float("inf")) == 1
+    assert _fwd(L, v=A + 8) == 3
+    assert _fwd(L, lse=A + 4) == 3
+    assert L.attn_fwd_f16(None, A, A, A, A, 1, 1, 1, 64, 0, 1.0, None) == 1
+
+
+def test_backward_argument_errors(L):
+    assert _bwd(L, dq=None) == 1
+    assert _bwd(L, acc=None) == 1
+    assert _bwd(L, H=0) == 1
+    assert _bwd(L, d=80) == 2
+    assert _bwd(L, scale=0.0) == 1
+    assert _bwd(L, dk=A + 2) == 3
+    assert _bwd(L, D=A + 8) == 3
+    assert L.attn_bwd_preprocess(None, A, A, A, 1, 1, 1, 64, None) == 1
+    assert L.attn_bwd_preprocess(A, A, A, A, 1, 1, 1, 48, None) == 2
+    assert L.attn_bwd_preprocess(A, A + 8, A, A, 1, 1, 1, 64, None) == 3
+    assert L.attn_selftest_timeout(0, None) == 1
+    assert L.attn_selftest_timeout(2000000, None) == 1
+
+
+def test_no_device_is_reported_not_faked(L):
+    """Without an sm_103 device a valid call reports UNSUPPORTED_DEVICE; there
+    is no CPU fallback."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(L) == 4
+    assert _bwd(L) == 4
+    with pytest.raises(attn.AttnError):
+        attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 64, False, 0.125, None)
+
+
+def test_torch_wrapper_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.forward(q, q, q)
+    with pytest.raises(ValueError):
+        attn.forward(q.float(), q.float(), q.float())
+
+
+def _imports(path):
+    tree = ast.parse(open(path).read())
+    mods = set()
+    for node in ast.walk(tree):
+        if isinstance(node, ast.Import):
+            mods |= {a.name.split(".")[0] for a in node.names}
+        elif isinstance(node, ast.ImportFrom) and node.module:
+            mods.add(node.module.split(".")[0])
+    return mods
+
+
+def test_product_and_oracle_are_independent():
+    for p in glob.glob(os.path.join(ROOT, "io_aware_exact_gb300", "*.py")):
+        assert "oracle" not in _imports(p), p
+    for p in glob.glob(os.path.join(ROOT, "io_aware_exact_gb300", "csrc", "*")):
+        assert "oracle" not in open(p).read().lower(), p
+    for p in glob.glob(os.path.join(ROOT, "oracle", "*.py")):
+        assert "io_aware_exact_gb300" not in _imports(p), p
+    assert "attn" not in open(os.path.join(ROOT, "oracle", "attn_oracle.c")).read().split(
+        "#include")[1].split("\n")[0]
+
+
+def test_library_allocates_nothing():
+    """The CUDA sources never call an allocator: every buffer is the caller's."""
+    for p in glob.glob(os.path.join(ROOT, "io_aware_exact_gb300", "csrc", "*")):
+        text = open(p).read()
+        for bad in (r"\bcudaMalloc", r"\bcudaFree", r"\bcuMemAlloc", r"\bmalloc\s*\(",
+                    r"=\s*new\b", r"\bcudaMallocAsync"):
+            assert not re.search(bad, text), (p, bad)

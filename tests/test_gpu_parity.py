@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Every case draws seeded bf16 inputs, runs the library on the GPU over the
+whole [B, H, N, d] problem (the same launch the benchmark times), and compares
+O, lse, dQ, dK, dV with the oracle on the same bf16 values: every head for the
+small shapes, sampled heads (and for N = 32768 sampled rows / key columns) for
+the large workloads.  Tolerances are those of ``tests/parity.py``.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import io_aware_exact_gb300 as attn
+from io_aware_exact_gb300.inputs import WORKLOADS, make_inputs
+from parity import check_lse, check_tensor, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _run_gpu(x, causal, scale, backward, f16=False):
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = attn.forward(q, k, v, causal, scale)
+    out = {"o": o, "lse": lse}
+    if backward:
+        dO = x["dO"].to(dev)
+        dq, dk, dv = attn.backward(q, k, v, o, lse, dO, causal, scale)
+        out.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    return {kk: vv.cpu() for kk, vv in out.items()}
+
+
+def _compare_head(x, out, b, h, causal, scale, backward, rows=None, cols=None, report=None):
+    q, k, v = (_f64(x[n][b, h]) for n in ("q", "k", "v"))
+    N = q.shape[0]
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, causal, scale, rows=rows)
+    sel = slice(None) if rows is None else rows
+    check_tensor("O", _f64(out["o"][b, h])[sel], o_ref, report)
+    check_lse(out["lse"][b, h].numpy().astype(np.float64)[sel], lse_ref, report)
+    if not backward:
+        return
+    dO = _f64(x["dO"][b, h])
+    if rows is None and cols is None:
+        dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward(q, k, v, dO, causal, scale)
+        check_tensor("dQ", _f64(out["dq"][b, h]), dq_ref, report)
+        check_tensor("dK", _f64(out["dk"][b, h]), dk_ref, report)
+        check_tensor("dV", _f64(out["dv"][b, h]), dv_ref, report)
+        return
+    _, _, dq_ref = oracle.attention_backward_rows(q, k, v, dO, causal, scale, rows=rows)
+    check_tensor("dQ", _f64(out["dq"][b, h])[rows], dq_ref, report)
+    lse_all, D_all, _ = oracle.attention_backward_rows(q, k, v, dO, causal, scale,
+                                                       with_dq=False)
+    dk_ref, dv_ref = oracle.attention_backward_cols(q, k, v, dO, lse_all, D_all, causal, scale,
+                                                    cols=cols)
+    check_tensor("dK", _f64(out["dk"][b, h])[cols], dk_ref, report)
+    check_tensor("dV", _f64(out["dv"][b, h])[cols], dv_ref, report)
+
+
+SMALL = [
+    # (B, H, N, d, causal)
+    (1, 1, 128, 64, False),
+    (1, 1, 128, 128, True),
+    (1, 2, 256, 128, False),
+    (2, 1, 384, 64, True),
+    (1, 1, 1, 64, False),
+    (1, 1, 1, 128, True),
+    (1, 1, 5, 64, True),
+    (1, 1, 127, 128, False),
+    (1, 1, 129, 64, True),
+    (1, 2, 200, 128, True),
+    (1, 1, 1000, 64, False),
+    (1, 1, 1000, 128, True),
+    (2, 2, 513, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_forward_small(B, H, N, d, causal):
+    x = make_inputs(B, H, N, d, seed=7 + N + d, with_grad=False)
+    out = _run_gpu(x, causal, d ** -0.5, backward=False)
+    for b in range(B):
+        for h in range(H):
+            _compare_head(x, out, b, h, causal, d ** -0.5, backward=False)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_backward_small(B, H, N, d, causal):
+    x = make_inputs(B, H, N, d, seed=11 + N + d)
+    out = _run_gpu(x, causal, d ** -0.5, backward=True)
+    for b in range(B):
+        for h in range(H):
+            _compare_head(x, out, b, h, causal, d ** -0.5, backward=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_not_inverse_sqrt_d(causal):
+    """A scale other than 1/sqrt(d) must enter both S and the gradients."""
+    x = make_inputs(1, 2, 300, 64, seed=5)
+    out = _run_gpu(x, causal, 0.3, backward=True)
+    for h in range(2):
+        _compare_head(x, out, 0, h, causal, 0.3, backward=True)
+
+
+def test_fp16_entry_points():
+    x = make_inputs(1, 2, 320, 128, seed=9, dtype=torch.float16)
+    out = _run_gpu(x, True, 128 ** -0.5, backward=True)
+    for h in range(2):
+        _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
+
+
+def test_peaked_rows_forward():
+    """Q, K scaled by 8: softmax rows close to one-hot stress the max/rescale."""
+    x = make_inputs(1, 2, 1024, 128, seed=13, qk_mult=8.0)
+    out = _run_gpu(x, True, 128 ** -0.5, backward=True)
+    for h in range(2):
+        _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
+
+
+# ---------------------------------------------------------------------------
+# The five named workloads at full size (sampled outputs for the large ones)
+# ---------------------------------------------------------------------------
+
+def _heads(w, n, seed):
+    rng = np.random.default_rng(seed)
+    all_h = [(b, h) for b in range(w.B) for h in range(w.H)]
+    picks = {all_h[0], all_h[-1]}
+    while len(picks) < min(n, len(all_h)):
+        picks.add(all_h[int(rng.integers(len(all_h)))])
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name,nheads", [
+    ("fwd_b1_h2_n256_d64", 2),
+    ("fwdbwd_b8_h16_n1024_d64", 8),
+    ("fwdbwd_causal_b4_h32_n4096_d128", 2),
+    ("fwdbwd_causal_peaked_b2_h16_n8192_d128", 2),
+])
+def test_workload(name, nheads):
+    w = WORKLOADS[name]
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_grad=w.backward)
+    out = _run_gpu(x, w.causal, w.scale, backward=w.backward)
+    for (b, h) in _heads(w, nheads, w.seed):
+        _compare_head(x, out, b, h, w.causal, w.scale, w.backward)
+
+
+def test_workload_long_sequence():
+    """N = 32768: one head, sampled query rows (O, lse, dQ) and key columns (dK, dV)."""
+    w = WORKLOADS["fwdbwd_causal_b1_h8_n32768_d128"]
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    out = _run_gpu(x, w.causal, w.scale, backward=True)
+    rows = sample_rows(w.N, 96, seed=1)
+    cols = sample_rows(w.N, 96, seed=2)
+    _compare_head(x, out, 0, w.H - 1, w.causal, w.scale, True, rows=rows, cols=cols)
+
+
+def test_no_nxn_buffer_long_sequence():
+    """The library allocates nothing: device free memory is unchanged by the calls
+    (an N x N fp32 score matrix for one head at N = 32768 would be 4 GiB)."""
+    w = WORKLOADS["fwdbwd_causal_b1_h8_n32768_d128"]
+    dev = torch.device("cuda:0")
+    x = {k: v.to(dev) for k, v in make_inputs(w.B, w.H, w.N, w.d, w.seed).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    D = torch.empty_like(lse)
+    acc = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    attn.forward(x["q"], x["k"], x["v"], True, None, o=o, lse=lse)
+    attn.backward(x["q"], x["k"], x["v"], o, lse, x["dO"], True, None, dq=dq, dk=dk, dv=dv,
+                  D=D, dq_accum=acc)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert attn.attn_get_device_status() == 0
+    assert abs(free0 - free1) < (64 << 20)
+
+
+def test_timeout_path_reports_and_context_survives():
+    """A wait that nothing completes runs out, is reported, and the GPU keeps
+    working (no trap, no hang)."""
+    attn.attn_selftest_timeout(2000)
+    assert attn.attn_get_device_status() == 6
+    assert attn.attn_get_device_status() == 0
+    x = make_inputs(1, 1, 128, 64, seed=3, with_grad=False)
+    out = _run_gpu(x, False, 0.125, backward=False)
+    _compare_head(x, out, 0, 0, False, 0.125, backward=False)
+
+
+def test_repeated_calls_deterministic_forward():
+    x = make_inputs(1, 4, 1024, 128, seed=21, with_grad=False)
+    a = _run_gpu(x, True, 128 ** -0.5, backward=False)
+    b = _run_gpu(x, True, 128 ** -0.5, backward=False)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
