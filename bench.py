@@ -1,0 +1,391 @@
+"""Benchmark: exact attention forward + backward on GB300.
+
+One step = one pass of the whole hot path over one batch: attn_fwd,
+attn_bwd_preprocess and attn_bwd (main kernel + dQ convert) on the causal
+B=2 H=16 N=8192 d=128 workload (Q, K scaled by 3 for peaked softmax rows),
+bf16 inputs resident in HBM.  FLOPs per step follow the stated convention:
+forward 4*B*H*N^2*d, forward+backward 10*B*H*N^2*d, each halved for causal.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  The reference arm (--impl reference) times
+the fp64 CPU oracle, as it stands, on the host cores over a bounded sample
+of the same workload (whole heads).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from io_aware_exact_gb300.inputs import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention TFLOPS fwd and fwd+bwd on 1 GB300, % of dense BF16 tensor peak"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d.get("bf16_tflops"), "bf16_tflops_sustained":
+                d.get("bf16_tflops_sustained"), "hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args):
+    import torch
+    import io_aware_exact_gb300 as attn
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = WORKLOADS[args.workload]
+    B, H, N, d, causal = w.B, w.H, w.N, w.d, w.causal
+    x = make_inputs(B, H, N, d, w.seed + 100 * rank, w.qk_mult)
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    D = torch.empty_like(lse)
+    acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    s = int(stream.cuda_stream)
+    scale = w.scale
+    P = lambda t: t.data_ptr()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+        if ev:
+            ev[1].record(stream)
+        attn.attn_bwd_preprocess(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), B, H, N, d,
+                                 causal, scale, s)
+        if ev:
+            ev[2].record(stream)
+        attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
+                      B, H, N, d, causal, scale, s)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between steps, outside the per-step events
+            step(evs[i])
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        wall = time.perf_counter() - t0
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during the timed steps")
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_fwd = [e[0].elapsed_time(e[1]) for e in evs]
+    t_pre = [e[1].elapsed_time(e[2]) for e in evs]
+    t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_step = sum(t_step) / len(t_step)
+    if pg:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if args.e2e_steps > 0:
+        hx = {kk: vv.pin_memory() for kk, vv in x.items()}
+        hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        dx = {kk: torch.empty_like(vv, device=dev) for kk, vv in x.items()}
+
+        def e2e_step():
+            for kk in dx:
+                dx[kk].copy_(hx[kk], non_blocking=True)
+            oo, ll = attn.forward(dx["q"], dx["k"], dx["v"], causal, scale, o=o, lse=lse)
+            attn.backward(dx["q"], dx["k"], dx["v"], oo, ll, dx["dO"], causal, scale,
+                          dq=dq, dk=dk, dv=dv, D=D, dq_accum=acc)
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                hout[n].copy_(t, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = ea.elapsed_time(eb) / args.e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+        e2e = {"value": round(world * w.flops_fwd_bwd() / (ms_e2e * 1e-3) / 1e12, 2),
+               "unit": "TFLOPS", "ms_per_step": round(ms_e2e, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks = _peaks()
+    flops_fb = w.flops_fwd_bwd()
+    tflops_fb = world * flops_fb / (ms_step * 1e-3) / 1e12
+    ms_fwd = statistics.mean(t_fwd)
+    ms_bwd = statistics.mean(t_bwd)
+    tflops_fwd = w.flops_fwd() / (ms_fwd * 1e-3) / 1e12
+    # dominant kernel: the backward main kernel (timed with its dQ convert);
+    # algorithmic work = 5 MMAs x 2 N^2 d per head, halved for causal
+    flops_bwd_kernel = 10.0 * B * H * N * N * d / (2 if causal else 1)
+    bwd_tflops = flops_bwd_kernel / (ms_bwd * 1e-3) / 1e12
+    peak_sus = peaks["bf16_tflops_sustained"]
+    peak_burst = peaks["bf16_tflops"]
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            tr = json.load(f)
+        if tr.get("workload") == args.workload and tr.get("kernel_rev") == KERNEL_REV:
+            traffic = tr.get("bytes_per_launch")
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(tflops_fb, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), Q and K x3, bf16)",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "global_batch": B * world, "seq_len": N,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs 268 MB > 126 MB L2, and L2 flushed (512 MB write) between steps",
+                   "flop_convention": "fwd 4BHN^2d, fwd+bwd 10BHN^2d, halved for causal"},
+        "frac_of_peak": round(tflops_fb / peak_sus, 4),
+        "fwd": {"tflops": round(tflops_fwd, 2), "ms": round(ms_fwd, 4),
+                "frac_of_peak": round(tflops_fwd / peak_burst, 4), "peak": peak_burst},
+        "fwd_bwd_14x_tflops": round(world * 14.0 * B * H * N * N * d / 2 / (ms_step * 1e-3) / 1e12, 2),
+        "bwd_preprocess_ms": round(statistics.mean(t_pre), 4),
+        "roofline": {"kernel": "attn_bwd (main kernel + dQ convert)", "bound": "tensor",
+                     "achieved": round(bwd_tflops, 2), "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": round(bwd_tflops / peak_sus, 4), "traffic": traffic,
+                     "peak_kind": "bf16 sustained, %s" % peaks["source"]},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+KERNEL_REV = "bwd-v1"
+
+
+def _oracle_step(w, x, heads):
+    """Oracle forward + backward of the given (b, h) heads; returns seconds."""
+    import numpy as np
+    import oracle
+    f = lambda t: t.float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        qh, kh, vh, dOh = (f(x[n][b, h]) for n in ("q", "k", "v", "dO"))
+        oracle.attention_forward(qh, kh, vh, w.causal, w.scale)
+        oracle.attention_backward(qh, kh, vh, dOh, w.causal, w.scale)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, nheads):
+    import oracle
+    oracle.build()
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    heads = [(0, h) for h in range(min(nheads, w.H))]
+    secs = _oracle_step(w, x, heads)
+    per_head = w.flops_fwd_bwd() / (w.B * w.H)
+    return {"value": round(per_head * len(heads) / secs / 1e12, 6), "unit": "TFLOPS",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of %d heads (b=0), all rows, fwd+bwd, %.1f s" % (
+                len(heads), w.B * w.H, secs)}
+
+
+def _ref_sample(w, x, rows, cols, lse_all, D_all):
+    """One reference step: the oracle's forward and backward row passes over
+    `rows` and its backward column pass over `cols` of head (0, 0)."""
+    import numpy as np
+    import oracle
+    f = lambda t: t.float().numpy().astype(np.float64)
+    qh, kh, vh, dOh = (f(x[n][0, 0]) for n in ("q", "k", "v", "dO"))
+    t0 = time.perf_counter()
+    oracle.attention_forward(qh, kh, vh, w.causal, w.scale, rows=rows)
+    oracle.attention_backward_rows(qh, kh, vh, dOh, w.causal, w.scale, rows=rows)
+    oracle.attention_backward_cols(qh, kh, vh, dOh, lse_all, D_all, w.causal, w.scale, cols=cols)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, timed on the host cores.
+
+    A step is a bounded sample of the workload: for head (0, 0), the last
+    256 query rows (forward + backward row pass) and the first 256 key
+    columns (backward column pass); those are the rows/columns with the most
+    visible (query, key) pairs under the causal mask.  Its FLOPs in the stated
+    convention are 10*d per visible pair, averaged over the row-side and
+    column-side pairs processed (for a whole head both equal N^2/2, giving
+    10*N^2*d/2).  The column pass needs every row's lse and D, which the
+    oracle computes once before timing.
+    """
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    n = min(256, w.N)
+    rows = np.arange(w.N - n, w.N, dtype=np.int64)
+    cols = np.arange(0, n, dtype=np.int64)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    qh, kh, vh, dOh = (f(x[nm][0, 0]) for nm in ("q", "k", "v", "dO"))
+    lse_all, D_all, _ = oracle.attention_backward_rows(qh, kh, vh, dOh, w.causal, w.scale,
+                                                       with_dq=False)
+    if w.causal:
+        row_pairs = float(np.sum(rows + 1))
+        col_pairs = float(np.sum(w.N - cols))
+    else:
+        row_pairs = col_pairs = float(n * w.N)
+    flops = 10.0 * w.d * (row_pairs + col_pairs) / 2.0
+    for _ in range(args.warmup):
+        _ref_sample(w, x, rows, cols, lse_all, D_all)
+    times = [_ref_sample(w, x, rows, cols, lse_all, D_all) for _ in range(args.steps)]
+    ms = 1000.0 * sum(times) / len(times)
+    value = round(flops / (ms * 1e-3) / 1e12, 6)
+    sample = ("head (0,0): last %d query rows (fwd + bwd row pass) and first %d key columns "
+              "(bwd column pass) per step" % (n, n))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, bf16 values)",
+            "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-heads", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

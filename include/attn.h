@@ -11,7 +11,7 @@
  *     (sj-techlog "FlashAttention 원 논문 해부", section "원 논문의 정의";
  *      wonbeomjang.kr FlashAttention-2 review, "개선 2: m과 l 대신 L만 저장")
  *
- *   D_i = sum_k dO_ik O_ik,  dS_ij = P_ij (dP_ij - D_i),  dP = dO V^T,
+ *   dP = dO V^T,  D_i = sum_j P_ij dP_ij,  dS_ij = P_ij (dP_ij - D_i),
  *   dV = P^T dO,  dQ = tau dS K,  dK = tau dS^T Q
  *     (FlashAttention-2 review, sections "Backward Pass"; the factor tau
  *      comes from S = tau Q K^T).
@@ -68,31 +68,43 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
- * Backward pre-processing (FlashAttention-2 review, "Backward Pass" of
- * FlashAttention-2: D_i = rowsum(dO_i o O_i) computed ahead of the main loop).
- * Reads o and dO [B,H,N,d]; writes D [B,H,N] and sets dq_accum [B,H,N,d] to
- * zero.  Must precede attn_bwd on the same stream.
+ * Backward pre-processing.  Computes the softmax-gradient row term
+ *   D_i = sum_j P_ij dP_ij,   P_ij = exp(s_ij - lse_i),   dP = dO V^T
+ * (wonbeomjang.kr FlashAttention-2 review, "Backward Pass": D_i is the sum
+ * over row i of P o dP, computed once ahead of the main loop) in fp32 from P
+ * recomputed tile by tile and dP on the tensor cores, writes it to D [B,H,N],
+ * and sets dq_accum [B,H,N,d] to zero.  Reads q, k, v, dO [B,H,N,d] and lse
+ * [B,H,N] (from attn_fwd with the same q, k, v, causal, scale).  Must precede
+ * attn_bwd on the same stream.
+ *
+ * The review also gives D_i = rowsum(dO_i o O_i); it is equal in exact
+ * arithmetic, but O exists only rounded to 16 bits, and on rows whose
+ * softmax is nearly one-hot dS = P (dP - D) cancels so that this rounding
+ * alone exceeds the library's gradient tolerance.  Evaluating the definition
+ * with the same fp32 P that attn_bwd uses avoids it, for the price of one
+ * extra pass over S and dP.
  */
-int attn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum,
-                        int B, int H, int N, int d, void* stream);
-int attn_bwd_preprocess_f16(const void* o, const void* dO, float* D, float* dq_accum,
-                            int B, int H, int N, int d, void* stream);
+int attn_bwd_preprocess(const void* q, const void* k, const void* v, const void* dO,
+                        const float* lse, float* D, float* dq_accum,
+                        int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_preprocess_f16(const void* q, const void* k, const void* v, const void* dO,
+                            const float* lse, float* D, float* dq_accum,
+                            int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
  * Backward pass (recomputation of S and P from lse, sj-techlog page, section
  * "forward가 끝난 뒤 backward는 무엇을 저장하고 무엇을 다시 계산하는가";
  * K/V-block outer loop of the FlashAttention-2 backward).  Reads q, k, v, dO
- * [B,H,N,d], lse and D [B,H,N] (from attn_fwd and attn_bwd_preprocess with the
- * same arguments), accumulates into dq_accum (zeroed by the preprocess), and
- * writes dq, dk, dv [B,H,N,d].  `o` is accepted for interface symmetry and may
- * be NULL.  dq_accum is left holding tau^-1 dQ in fp32 (unspecified to
- * callers).
+ * [B,H,N,d], lse and D [B,H,N] (from attn_fwd and attn_bwd_preprocess with
+ * the same arguments), accumulates dS K into dq_accum (zeroed by the
+ * preprocess) with fp32 atomics, and writes dq, dk, dv [B,H,N,d].
+ * dq_accum is left holding dQ / scale.
  */
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+int attn_bwd(const void* q, const void* k, const void* v, const void* dO,
              const float* lse, const float* D, float* dq_accum,
              void* dq, void* dk, void* dv,
              int B, int H, int N, int d, int causal, float scale, void* stream);
-int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO,
                  const float* lse, const float* D, float* dq_accum,
                  void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, int causal, float scale, void* stream);

@@ -51,8 +51,8 @@ def lib():
             L = ctypes.CDLL(LIB_PATH)
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             fwd = [P, P, P, P, P, I, I, I, I, I, F, P]
-            pre = [P, P, P, P, I, I, I, I, P]
-            bwd = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+            pre = [P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+            bwd = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
             for name, at in (("attn_fwd", fwd), ("attn_fwd_f16", fwd),
                              ("attn_bwd_preprocess", pre), ("attn_bwd_preprocess_f16", pre),
                              ("attn_bwd", bwd), ("attn_bwd_f16", bwd)):
@@ -100,15 +100,17 @@ def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream, f16=False):
            "attn_fwd")
 
 
-def attn_bwd_preprocess(o, dO, D, dq_accum, B, H, N, d, stream, f16=False):
+def attn_bwd_preprocess(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream,
+                        f16=False):
     fn = lib().attn_bwd_preprocess_f16 if f16 else lib().attn_bwd_preprocess
-    _check(fn(o, dO, D, dq_accum, B, H, N, d, stream), "attn_bwd_preprocess")
+    _check(fn(q, k, v, dO, lse, D, dq_accum, B, H, N, d, int(bool(causal)), float(scale), stream),
+           "attn_bwd_preprocess")
 
 
-def attn_bwd(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+def attn_bwd(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
              f16=False):
     fn = lib().attn_bwd_f16 if f16 else lib().attn_bwd
-    _check(fn(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, int(bool(causal)),
+    _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, int(bool(causal)),
               float(scale), stream), "attn_bwd")
 
 
@@ -164,9 +166,13 @@ def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=None, dv=None,
              D=None, dq_accum=None, stream=None):
-    """dQ, dK, dV for [B,H,N,d] CUDA tensors (workspace allocated by torch if not given)."""
+    """dQ, dK, dV for [B,H,N,d] CUDA tensors (workspace allocated by torch if not given).
+
+    ``o`` (the forward output) is not read and may be None: the preprocess
+    recomputes D from q, k, v, dO and lse.
+    """
     torch = _torch()
-    (B, H, N, d), f16 = _check_qkv(q, k, v, o, dO)
+    (B, H, N, d), f16 = _check_qkv(q, k, v, dO)
     scale = d ** -0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -175,11 +181,11 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
     if dq_accum is None:
         dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
     s = _stream_handle(stream)
-    attn_bwd_preprocess(o.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(),
-                        B, H, N, d, s, f16)
-    attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-             lse.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-             dv.data_ptr(), B, H, N, d, causal, scale, s, f16)
+    attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                        D.data_ptr(), dq_accum.data_ptr(), B, H, N, d, causal, scale, s, f16)
+    attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+             D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+             B, H, N, d, causal, scale, s, f16)
     return dq, dk, dv
 
 
@@ -189,7 +195,7 @@ def _autograd_function():
     class AttnFunction(torch.autograd.Function):
         """Exact attention with the library's forward and backward kernels.
 
-        Saves q, k, v, o and lse (O(N) extra per row, no N x N buffer) and
+        Saves q, k, v and lse (O(N) extra per row, no N x N buffer) and
         recomputes P in the backward, like the FlashAttention autograd
         function described on the sj-techlog page ("1. Python interface는
         scale·RNG state·작은 통계를 autograd에 넘긴다").
@@ -199,14 +205,14 @@ def _autograd_function():
         def forward(ctx, q, k, v, causal=False, scale=None):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
             o, lse = forward(q, k, v, causal, scale)
-            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.save_for_backward(q, k, v, lse)
             ctx.causal, ctx.scale = causal, scale
             return o
 
         @staticmethod
         def backward(ctx, dO):
-            q, k, v, o, lse = ctx.saved_tensors
-            dq, dk, dv = backward(q, k, v, o, lse, dO.contiguous(), ctx.causal, ctx.scale)
+            q, k, v, lse = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, None, lse, dO.contiguous(), ctx.causal, ctx.scale)
             return dq, dk, dv, None, None
 
     return AttnFunction

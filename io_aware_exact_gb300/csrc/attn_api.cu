@@ -132,28 +132,38 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
                                  static_cast<cudaStream_t>(stream)));
 }
 
-int pre_impl(const void* o, const void* dO, float* D, float* dq_accum, int B, int H, int N, int d,
+int pre_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+             float* D, float* dq_accum, int B, int H, int N, int d, int causal, float scale,
              void* stream, bool bf16) {
-    if (!o || !dO || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !dO || !lse || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
-    if (!aligned16(o) || !aligned16(dO) || !aligned16(D) || !aligned16(dq_accum))
+    if ((rc = check_scale(scale))) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+        !aligned16(D) || !aligned16(dq_accum))
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    BwdPreArgs a{};
-    a.o = o;
-    a.dO = dO;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
+        return rc;
+    DsumArgs a{};
+    a.lse = lse;
     a.D = D;
     a.dq_accum = dq_accum;
-    a.rows = static_cast<long long>(B) * H * N;
-    a.d = d;
-    return map_launch(launch_bwd_preprocess(a, bf16, static_cast<cudaStream_t>(stream)));
+    a.status = status;
+    a.N = N;
+    a.scale_log2 = scale * kLog2e;
+    a.timeout_ns = kDefaultTimeoutNs;
+    return map_launch(launch_bwd_preprocess(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
-int bwd_impl(const void* q, const void* k, const void* v, const void* /*o*/, const void* dO,
-             const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
-             int B, int H, int N, int d, int causal, float scale, void* stream, bool bf16) {
+int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+             const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int N,
+             int d, int causal, float scale, void* stream, bool bf16) {
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
@@ -225,28 +235,30 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
     return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, stream, false);
 }
 
-int attn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum, int B, int H,
-                        int N, int d, void* stream) {
-    return pre_impl(o, dO, D, dq_accum, B, H, N, d, stream, true);
+int attn_bwd_preprocess(const void* q, const void* k, const void* v, const void* dO,
+                        const float* lse, float* D, float* dq_accum, int B, int H, int N, int d,
+                        int causal, float scale, void* stream) {
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream, true);
 }
 
-int attn_bwd_preprocess_f16(const void* o, const void* dO, float* D, float* dq_accum, int B,
-                            int H, int N, int d, void* stream) {
-    return pre_impl(o, dO, D, dq_accum, B, H, N, d, stream, false);
+int attn_bwd_preprocess_f16(const void* q, const void* k, const void* v, const void* dO,
+                            const float* lse, float* D, float* dq_accum, int B, int H, int N,
+                            int d, int causal, float scale, void* stream) {
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream, false);
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-             const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
-             int B, int H, int N, int d, int causal, float scale, void* stream) {
-    return bwd_impl(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale,
-                    stream, true);
+int attn_bwd(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+             const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int N,
+             int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+                    true);
 }
 
-int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                 const float* lse, const float* D, float* dq_accum, void* dq, void* dk, void* dv,
-                 int B, int H, int N, int d, int causal, float scale, void* stream) {
-    return bwd_impl(q, k, v, o, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale,
-                    stream, false);
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                 const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H,
+                 int N, int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+                    false);
 }
 
 const char* attn_status_string(int s) {

@@ -1,9 +1,9 @@
 // attn_bwd.cu - exact attention backward for sm_103a (TMA + tcgen05 + TMEM).
 //
 // Three kernels, launched in this order on the caller's stream:
-//  1. preprocess: D_i = sum_k dO_ik O_ik (fp32) and dq_accum := 0
-//     (wonbeomjang.kr FlashAttention-2 review, "Backward Pass" of
-//     FlashAttention-2: D is computed ahead of the main loop);
+//  1. preprocess: D_i = sum_j P_ij dP_ij in fp32 and dq_accum := 0
+//     (wonbeomjang.kr FlashAttention-2 review, "Backward Pass": D is the
+//     softmax-gradient row term, computed ahead of the main loop);
 //  2. main kernel, K/V-block outer loop (same review: each CTA owns dK_j, dV_j
 //     and needs no inter-CTA synchronisation; dQ is accumulated across CTAs
 //     with atomic adds).  Per (b, h, 128-key block j), for each 128-query
@@ -34,41 +34,6 @@
 namespace attn {
 
 // ============================================================================
-// 1. preprocess
-// ============================================================================
-template <bool BF16, int D>
-__global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(const BwdPreArgs a) {
-    constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
-    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-    const int sub = threadIdx.x % TPR;
-    const long long rows_per_sweep = nthreads / TPR;
-    const long long sweeps = (a.rows + rows_per_sweep - 1) / rows_per_sweep;
-    // every thread runs the same number of sweeps, so the row-group shuffles
-    // below always see all 32 lanes of the warp
-    for (long long sw = 0; sw < sweeps; ++sw) {
-        const long long row = sw * rows_per_sweep + tid / TPR;
-        const bool valid = row < a.rows;
-        float acc = 0.f;
-        if (valid) {
-            const uint4 o4 = reinterpret_cast<const uint4*>(a.o)[row * TPR + sub];
-            const uint4 d4 = reinterpret_cast<const uint4*>(a.dO)[row * TPR + sub];
-            const uint16_t* oh = reinterpret_cast<const uint16_t*>(&o4);
-            const uint16_t* dh = reinterpret_cast<const uint16_t*>(&d4);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(to_f32<BF16>(oh[e]), to_f32<BF16>(dh[e]), acc);
-            float4* z = reinterpret_cast<float4*>(a.dq_accum + row * D + sub * 8);
-            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
-        if (valid && sub == 0) a.D[row] = acc;
-    }
-}
-
-// ============================================================================
 // 3. dQ convert
 // ============================================================================
 template <bool BF16>
@@ -85,6 +50,248 @@ __global__ void __launch_bounds__(256) attn_dq_convert_kernel(const DqConvertArg
         r.z = pack2<BF16>(y.x * a.scale, y.y * a.scale);
         r.w = pack2<BF16>(y.z * a.scale, y.w * a.scale);
         reinterpret_cast<uint4*>(a.dq)[i] = r;
+    }
+}
+
+// ============================================================================
+// 1. preprocess: exact D_i = sum_j P_ij dP_ij, and dq_accum := 0
+// ============================================================================
+// D is the definition of the softmax-gradient row term (FlashAttention-2
+// review, "Backward Pass": D_i = sum_j P_ij dP_ij = (P_i o dP_i)^T 1).  The
+// review's shortcut rowsum(dO o O) (computed by the preprocess kernel) uses O
+// after its rounding to 16 bits; on rows whose softmax is close to one-hot the
+// factor dP_ij - D_i of dS cancels and that rounding dominates dQ.  This pass
+// recomputes P from lse in fp32 and dP = dO V^T on the tensor cores and sums
+// their product per row, so dS = P (dP - D) below uses the same fp32 P and a
+// matching D.
+//
+// One CTA = one (b, h) and 128 query rows; K/V blocks stream through a TMA
+// ring; S and dP of a block land in one of two TMEM buffers so the MMAs of
+// block j+1 run while the compute warpgroups reduce block j.  Warpgroup c
+// (warps 4+4c .. 7+4c) handles key columns [64c, 64c+64) of each block.
+template <int D>
+struct DsumCfg {
+    static constexpr int STAGES = (D == 128) ? 2 : 4;
+    static constexpr int KBOX = D / kBoxCols;
+    static constexpr int TILE_BYTES = kTile * D * 2;
+    static constexpr int Q_OFF = 0;
+    static constexpr int DO_OFF = Q_OFF + TILE_BYTES;
+    static constexpr int K_OFF = DO_OFF + TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+    static constexpr int RED_OFF = V_OFF + STAGES * TILE_BYTES;   // 128 floats
+    static constexpr int BAR_OFF = RED_OFF + kTile * 4;
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_VFULL = B_KFULL + STAGES;
+    static constexpr int B_KVEMPTY = B_VFULL + STAGES;
+    static constexpr int B_SDP = B_KVEMPTY + STAGES;       // [2]
+    static constexpr int B_FREE = B_SDP + 2;               // [2] buffer consumed
+    static constexpr int B_RED = B_FREE + 2;               // warpgroup 1 partial sums ready
+    static constexpr int B_DRAIN = B_RED + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    __device__ static constexpr uint32_t s_col(int b) { return 256u * b; }
+    __device__ static constexpr uint32_t dp_col(int b) { return 256u * b + 128u; }
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const DsumArgs args) {
+    using C = DsumCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int N = args.N;
+    const int nblk = (N + kTile - 1) / kTile;
+    const int qi = nblk - 1 - static_cast<int>(blockIdx.y);     // heavy query blocks first
+    const int nkv = CAUSAL ? min(nblk, qi + 1) : nblk;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::B_SDP + b), 1);
+            mbar_init(bar(C::B_FREE + b), 256);
+        }
+        mbar_init(bar(C::B_RED), 128);
+        mbar_init(bar(C::B_DRAIN), 1);
+        *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const bool skip = *abort_flag != 0;
+
+    if (!skip && warp >= 2) {
+        // dq_accum := 0 for this CTA's 128 rows (a contiguous 128 x d fp32 block),
+        // coalesced, by the warps that are otherwise idle until the first MMA
+        const int rows = min(kTile, N - qi * kTile);
+        float4* z = reinterpret_cast<float4*>(args.dq_accum +
+                                              (static_cast<size_t>(bh) * N + qi * kTile) * D);
+        const int n4 = rows * D / 4;
+        for (int e = threadIdx.x - 64; e < n4; e += C::THREADS - 64) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    if (skip) {
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
+            for (int b = 0; b < C::KBOX; ++b) {
+                tma_load_3d(sbase + C::Q_OFF + b * kBoxBytes, &tm_q, bar(C::B_QFULL), b * kBoxCols,
+                            qi * kTile, bh, pol_q);
+                tma_load_3d(sbase + C::DO_OFF + b * kBoxBytes, &tm_do, bar(C::B_QFULL),
+                            b * kBoxCols, qi * kTile, bh, pol_q);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                if (j >= C::STAGES) {
+                    ok = wait_bar(wc, bar(C::B_KVEMPTY + s), ((j / C::STAGES) - 1) & 1);
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
+                                bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
+                for (int b = 0; b < C::KBOX; ++b)
+                    tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
+                                bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                issued = j + 1;
+            }
+            if (!ok) {
+                drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
+                for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+                    drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                    drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = BF16 ? 1u : 0u;
+            constexpr uint32_t id = idesc_f16(128, 128, fmt, 0, 0);  // Q K^T and dO V^T
+            bool ok = wait_bar(wc, bar(C::B_QFULL), 0);
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const int b = j & 1;
+                if (!(ok = wait_bar(wc, bar(C::B_KFULL + s), (j / C::STAGES) & 1))) break;
+                if (j >= 2 && !(ok = wait_bar(wc, bar(C::B_FREE + b), ((j >> 1) - 1) & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::s_col(b),
+                           smem_desc(sbase + C::Q_OFF + off, 16, 1024, LAYOUT_SW128),
+                           smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES + off, 16, 1024, LAYOUT_SW128),
+                           id, kk > 0);
+                }
+                if (!(ok = wait_bar(wc, bar(C::B_VFULL + s), (j / C::STAGES) & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::dp_col(b),
+                           smem_desc(sbase + C::DO_OFF + off, 16, 1024, LAYOUT_SW128),
+                           smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES + off, 16, 1024, LAYOUT_SW128),
+                           id, kk > 0);
+                }
+                mma_commit(bar(C::B_SDP + b));
+                mma_commit(bar(C::B_KVEMPTY + s));
+            }
+            mma_commit(bar(C::B_DRAIN));
+            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ row sums
+        const int c = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int row = qi * kTile + r;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const float cs = args.scale_log2;
+        const float nl2 = (row < N) ? -args.lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
+        float acc0 = 0.f, acc1 = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int b = j & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SDP + b), (j >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            // keys >= limit are masked: the key tail and, on the diagonal block, keys > row
+            int limit = N - (j * kTile + 64 * c);
+            if (CAUSAL) limit = min(limit, row - (j * kTile + 64 * c) + 1);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c + 32 * h, sr);
+                tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c + 32 * h, dr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), cs, nl2));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), cs, nl2));
+                    if (32 * h + e >= limit) p0 = 0.f;
+                    if (32 * h + e + 1 >= limit) p1 = 0.f;
+                    acc0 = fmaf(p0, __uint_as_float(dr[e]), acc0);
+                    acc1 = fmaf(p1, __uint_as_float(dr[e + 1]), acc1);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::B_FREE + b));
+        }
+        const float acc = acc0 + acc1;
+        if (c == 1) {
+            red[r] = acc;
+            mbar_arrive(bar(C::B_RED));
+        } else if (ok) {
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_RED), 0));
+            if (ok && row < N) args.D[static_cast<size_t>(bh) * N + row] = acc + red[r];
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -400,38 +607,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             const int qrow = i * kTile + r;
             float* dq_row = args.dq_accum + (static_cast<size_t>(bh) * N + qrow) * D;
-            if constexpr (D == 128) {
+            // Read this warpgroup's dQ columns out of TMEM, release the columns to
+            // the MMA issuer at once, then add them to dq_accum while the next
+            // tile's MMAs already run.
+            constexpr int NQ = D / 2;                 // dQ columns per warpgroup
+            uint32_t q32[NQ];
+            const uint32_t qcol = (D == 128) ? C::dq_col(c) : C::dq_col(0) + 32 * c;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t q32[32];
-                    tmem_ld32(tmem + lane_off + C::dq_col(c) + 32 * h, q32);
-                    tmem_ld_wait();
-                    if (qrow < N) {
-                        float4* dst = reinterpret_cast<float4*>(dq_row + 64 * c + 32 * h);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
-                                                            __uint_as_float(q32[4 * v4 + 1]),
-                                                            __uint_as_float(q32[4 * v4 + 2]),
-                                                            __uint_as_float(q32[4 * v4 + 3])));
-                    }
-                }
-            } else {
-                uint32_t q32[32];
-                tmem_ld32(tmem + lane_off + C::dq_col(0) + 32 * c, q32);
-                tmem_ld_wait();
-                if (qrow < N) {
-                    float4* dst = reinterpret_cast<float4*>(dq_row + 32 * c);
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
-                                                        __uint_as_float(q32[4 * v4 + 1]),
-                                                        __uint_as_float(q32[4 * v4 + 2]),
-                                                        __uint_as_float(q32[4 * v4 + 3])));
-                }
-            }
+            for (int h = 0; h < NQ / 32; ++h)
+                tmem_ld32(tmem + lane_off + qcol + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(bar(C::B_DQEMPTY));
+            if (qrow < N) {
+                float4* dst = reinterpret_cast<float4*>(dq_row + NQ * c);
+#pragma unroll
+                for (int v4 = 0; v4 < NQ / 4; ++v4)
+                    atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
+                                                    __uint_as_float(q32[4 * v4 + 1]),
+                                                    __uint_as_float(q32[4 * v4 + 2]),
+                                                    __uint_as_float(q32[4 * v4 + 3])));
+            }
         }
         // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
@@ -483,24 +679,6 @@ static int sm_count() {
     return n;
 }
 
-cudaError_t launch_bwd_preprocess(const BwdPreArgs& a, bool bf16, cudaStream_t stream) {
-    const long long rows_per_block = 256 / (a.d / 8);
-    long long blocks = (a.rows + rows_per_block - 1) / rows_per_block;
-    const long long cap = static_cast<long long>(sm_count()) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    if (a.d == 64) {
-        if (bf16) attn_bwd_preprocess_kernel<true, 64><<<blocks, 256, 0, stream>>>(a);
-        else attn_bwd_preprocess_kernel<false, 64><<<blocks, 256, 0, stream>>>(a);
-    } else if (a.d == 128) {
-        if (bf16) attn_bwd_preprocess_kernel<true, 128><<<blocks, 256, 0, stream>>>(a);
-        else attn_bwd_preprocess_kernel<false, 128><<<blocks, 256, 0, stream>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
-}
-
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream) {
     long long blocks = (a.elems / 8 + 255) / 256;
     const long long cap = static_cast<long long>(sm_count()) * 8;
@@ -523,6 +701,37 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     dim3 grid(BH, a.num_kvblocks);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool BF16>
+static cudaError_t launch_pre_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const DsumArgs& a, int BH,
+                                 cudaStream_t stream) {
+    using C = DsumCfg<D>;
+    auto kern = attn_bwd_dsum_kernel<D, CAUSAL, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(BH, (a.N + kTile - 1) / kTile);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const DsumArgs& a, int BH, int d, bool causal,
+                            bool bf16, cudaStream_t stream) {
+#define ATTN_PRE_CASE(D_, C_, B_) \
+    if (d == D_ && causal == C_ && bf16 == B_) return launch_pre_t<D_, C_, B_>(tq, tk, tv, tdo, a, BH, stream);
+    ATTN_PRE_CASE(64, false, true)
+    ATTN_PRE_CASE(64, true, true)
+    ATTN_PRE_CASE(128, false, true)
+    ATTN_PRE_CASE(128, true, true)
+    ATTN_PRE_CASE(64, false, false)
+    ATTN_PRE_CASE(64, true, false)
+    ATTN_PRE_CASE(128, false, false)
+    ATTN_PRE_CASE(128, true, false)
+#undef ATTN_PRE_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -29,15 +29,6 @@ struct FwdArgs {
     unsigned long long timeout_ns;
 };
 
-struct BwdPreArgs {
-    const void* o;         // [B*H, N, d]
-    const void* dO;        // [B*H, N, d]
-    float* D;              // [B*H, N]
-    float* dq_accum;       // [B*H, N, d] fp32, zeroed
-    long long rows;        // B*H*N
-    int d;
-};
-
 struct BwdArgs {
     const float* lse;      // [B*H, N]
     const float* D;        // [B*H, N]
@@ -48,6 +39,16 @@ struct BwdArgs {
     int N;
     int num_kvblocks;      // ceil(N / 128)
     float scale;           // softmax scale (tau)
+    float scale_log2;      // tau * log2(e)
+    unsigned long long timeout_ns;
+};
+
+struct DsumArgs {
+    const float* lse;      // [B*H, N]
+    float* D;              // [B*H, N], written: sum_j P_ij dP_ij
+    float* dq_accum;       // [B*H, N, d] fp32, zeroed
+    int* status;
+    int N;
     float scale_log2;      // tau * log2(e)
     unsigned long long timeout_ns;
 };
@@ -63,10 +64,12 @@ struct DqConvertArgs {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int BH, int d, bool causal, bool bf16,
                        cudaStream_t stream);
-cudaError_t launch_bwd_preprocess(const BwdPreArgs& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdArgs& a, int BH, int d, bool causal,
                        bool bf16, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const DsumArgs& a, int BH, int d, bool causal,
+                            bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -277,19 +277,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 l *= alpha;
                 m_ref = m_new;
             }
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // O holds P V up to block j-1 (S of block j was committed after it)
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t orr[32];
-                    tmem_ld32(o_addr + c, orr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(o_addr + c, orr);
-                }
-            }
             const float nm = -m_ref;
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
@@ -306,6 +293,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_st32(s_addr + 32 * h, pk);
             }
             l += sum0 + sum1;
+            // Rescale O after the P stores, when the S registers are dead.  O holds
+            // P V up to block j-1 (S of block j was committed after that MMA).
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(o_addr + c, orr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                    tmem_st32(o_addr + c, orr);
+                }
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL + t));

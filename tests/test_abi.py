@@ -46,12 +46,20 @@ def _fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, scale=0.
 
 
 def _bwd(L, **kw):
-    a = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, D=A, acc=A, dq=A, dk=A, dv=A, B=1, H=1, N=128,
+    a = dict(q=A, k=A, v=A, dO=A, lse=A, D=A, acc=A, dq=A, dk=A, dv=A, B=1, H=1, N=128,
              d=64, causal=0, scale=0.125)
     a.update(kw)
-    return L.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["D"], a["acc"],
+    return L.attn_bwd(a["q"], a["k"], a["v"], a["dO"], a["lse"], a["D"], a["acc"],
                       a["dq"], a["dk"], a["dv"], a["B"], a["H"], a["N"], a["d"], a["causal"],
                       a["scale"], None)
+
+
+def _pre(L, **kw):
+    a = dict(q=A, k=A, v=A, dO=A, lse=A, D=A, acc=A, B=1, H=1, N=128, d=64, causal=0,
+             scale=0.125)
+    a.update(kw)
+    return L.attn_bwd_preprocess(a["q"], a["k"], a["v"], a["dO"], a["lse"], a["D"], a["acc"],
+                                 a["B"], a["H"], a["N"], a["d"], a["causal"], a["scale"], None)
 
 
 def test_forward_argument_errors(L):
@@ -80,9 +88,11 @@ def test_backward_argument_errors(L):
     assert _bwd(L, scale=0.0) == 1
     assert _bwd(L, dk=A + 2) == 3
     assert _bwd(L, D=A + 8) == 3
-    assert L.attn_bwd_preprocess(None, A, A, A, 1, 1, 1, 64, None) == 1
-    assert L.attn_bwd_preprocess(A, A, A, A, 1, 1, 1, 48, None) == 2
-    assert L.attn_bwd_preprocess(A, A + 8, A, A, 1, 1, 1, 64, None) == 3
+    assert _pre(L, lse=None) == 1
+    assert _pre(L, d=48) == 2
+    assert _pre(L, dO=A + 8) == 3
+    assert _pre(L, scale=-2.0) == 1
+    assert _pre(L, N=0) == 1
     assert L.attn_selftest_timeout(0, None) == 1
     assert L.attn_selftest_timeout(2000000, None) == 1
 
@@ -95,6 +105,7 @@ def test_no_device_is_reported_not_faked(L):
         pytest.skip("a GPU is present")
     assert _fwd(L) == 4
     assert _bwd(L) == 4
+    assert _pre(L) == 4
     with pytest.raises(attn.AttnError):
         attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 64, False, 0.125, None)
 
