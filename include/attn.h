@@ -52,7 +52,8 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED_DEVICE = 4,   /* current device is not sm_103 */
     ATTN_ERR_LAUNCH = 5,               /* CUDA launch / driver error */
     ATTN_ERR_TIMEOUT = 6,              /* a kernel's bounded wait ran out */
-    ATTN_ERR_DEVICE_FAULT = 7          /* CUDA reported an error while syncing */
+    ATTN_ERR_DEVICE_FAULT = 7,         /* CUDA reported an error while syncing */
+    ATTN_ERR_SCRATCH_TOO_SMALL = 8     /* problem too large for attn_bwd_noalloc */
 } attn_status;
 
 /*
@@ -108,6 +109,35 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO,
                  const float* lse, const float* D, float* dq_accum,
                  void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Backward pass without caller-provided workspace (bf16).  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory at the time of the call, for example code running while a
+ * CUDA graph is captured (an allocation would invalidate the capture),
+ * plug-ins whose host framework owns all allocations, or real-time programs
+ * that allocate nothing after start-up.
+ *
+ * Computes exactly what attn_bwd_preprocess followed by attn_bwd compute,
+ * reading q, k, v, dO [B,H,N,d] and lse [B,H,N] and writing dq, dk, dv
+ * [B,H,N,d], but keeps D and the fp32 dQ accumulator in a fixed 16 MiB
+ * device array that the library reserves on every GPU that loads it, until
+ * the process exits.  It allocates nothing.
+ *  - Size limit: ceil(B*H*N / 64) * 64 + B*H*N*d <= 4194304 (fp32 elements),
+ *    e.g. B*H*N <= 32513 at d = 128 and <= 64527 at d = 64.  Larger problems
+ *    return ATTN_ERR_SCRATCH_TOO_SMALL with nothing enqueued.
+ *  - The first call on a device looks the array's device address up (once
+ *    per device, with that device current); make that first call before
+ *    capturing a stream into a graph.
+ *  - All calls on a device share the one array.  Each call overwrites D and
+ *    zeroes the accumulator before use, so earlier contents do not matter,
+ *    but calls whose kernels overlap on the GPU (different streams without
+ *    ordering between them) race on the array and give wrong results.
+ * Other conventions (alignment, errors, stream semantics) as for attn_bwd.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv,
+                     int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /* Static English description of a status code. */
 const char* attn_status_string(int status);

@@ -271,6 +271,7 @@ const char* attn_status_string(int s) {
         case ATTN_ERR_LAUNCH: return "CUDA launch failed";
         case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
         case ATTN_ERR_DEVICE_FAULT: return "CUDA reported an error while synchronising";
+        case ATTN_ERR_SCRATCH_TOO_SMALL: return "problem too large for the fixed no-allocation scratch array";
         default: return "unknown status";
     }
 }
