@@ -103,6 +103,24 @@ int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) 
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
 }
 
+// 3-D tensor map over the fp32 dQ accumulator [BH, N, d]: box = 32 columns
+// (128 bytes) x 128 rows x 1 head, 128-byte swizzle; rows beyond N of a head
+// are never written by a reduction through it.
+int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return ATTN_ERR_LAUNCH;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                   static_cast<cuuint64_t>(N) * d * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTile), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
 int map_launch(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -125,6 +143,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     a.lse = lse;
     a.status = status;
     a.N = N;
+    a.BH = BH;
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
     a.scale_log2 = scale * kLog2e;
     a.timeout_ns = kDefaultTimeoutNs;
@@ -155,6 +174,7 @@ int pre_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.dq_accum = dq_accum;
     a.status = status;
     a.N = N;
+    a.BH = BH;
     a.scale_log2 = scale * kLog2e;
     a.timeout_ns = kDefaultTimeoutNs;
     return map_launch(launch_bwd_preprocess(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16,
@@ -180,6 +200,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
         (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
         return rc;
+    CUtensorMap tdq;
+    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     BwdArgs a{};
     a.lse = lse;
@@ -189,11 +211,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.dv = dv;
     a.status = status;
     a.N = N;
+    a.BH = BH;
     a.num_kvblocks = (N + kTile - 1) / kTile;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.timeout_ns = kDefaultTimeoutNs;
-    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16, st))))
+    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, a, BH, d, causal != 0, bf16, st))))
         return rc;
     DqConvertArgs c{};
     c.dq_accum = dq_accum;

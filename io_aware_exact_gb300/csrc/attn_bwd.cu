@@ -6,29 +6,18 @@
 //     softmax-gradient row term, computed ahead of the main loop);
 //  2. main kernel, K/V-block outer loop (same review: each CTA owns dK_j, dV_j
 //     and needs no inter-CTA synchronisation; dQ is accumulated across CTAs
-//     with atomic adds).  Per (b, h, 128-key block j), for each 128-query
+//     by reduce-adds, here TMA tensor reductions into an fp32 buffer).  Per (b, h, 128-key block j), for each 128-query
 //     block i that can see block j:
 //        S^T  = K_j Q_i^T              (recomputed; sj-techlog "FlashAttention
 //        dP^T = V_j dO_i^T              원 논문 해부", backward section)
 //        P^T  = exp(tau S^T - lse_i)   (FlashAttention-2 review, "개선 2")
 //        dS^T = P^T o (dP^T - D_i)     (review, "Backward Pass": softmax grad)
-//        dQ_i += dS_ij K_j   (fp32 atomics into dq_accum)
+//        dQ_i += dS_ij K_j   (fp32 reduce-adds into dq_accum)
 //        dV_j += P^T dO_i,   dK_j += dS^T Q_i
 //     and finally dK_j *= tau (S = tau Q K^T);
 //  3. convert: dQ = tau * dq_accum, rounded to the 16-bit type.
 //
-// GB300 mapping of the main kernel (our design):
-//  * TMEM (512 columns): S^T at 0, dP^T at 128, dV at 256, dK at 256 + d.
-//    P^T (16-bit pairs) overwrites S^T columns [0,64) and dS^T overwrites
-//    dP^T columns [128,192); both feed the dV / dK MMAs straight from TMEM.
-//    dQ_i = dS K_j lands in the freed columns [64,128) (d columns 0..63) and
-//    [192,256) (d columns 64..127), is read out and atomically added.
-//  * dS^T is also written to shared memory (128-byte swizzle) as the
-//    MN-major A operand of the dQ MMA.
-//  * warp 0: TMA (K_j, V_j once; Q_i, dO_i through a ring), warp 1: MMA
-//    issuer, warp 2: TMEM owner, warp 3: loads lse_i, D_i into shared memory,
-//    warps 4-11: two compute warpgroups, each one key per thread (TMEM lane)
-//    and half of the 128 query columns.
+// GB300 mapping of the main kernel: see the comment above BwdCfg.
 #include "attn_common.cuh"
 
 namespace attn {
@@ -115,10 +104,11 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+    const int bh = grid_head();
+    if (bh >= args.BH) return;                   // padding of the last grid z-slice
     const int N = args.N;
     const int nblk = (N + kTile - 1) / kTile;
-    const int qi = nblk - 1 - static_cast<int>(blockIdx.y);     // heavy query blocks first
+    const int qi = nblk - 1 - static_cast<int>(blockIdx.x);     // heavy query blocks first
     const int nkv = CAUSAL ? min(nblk, qi + 1) : nblk;
 
     if (threadIdx.x == 0) {
@@ -298,6 +288,22 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 // ============================================================================
 // 2. main backward kernel
 // ============================================================================
+// One CTA = one (b, h) and one 128-key block j; it loops over the 128-query
+// blocks i that can see block j and keeps dV_j, dK_j in TMEM.  Per block i:
+//
+//   MMA:   S^T = K Q_i^T, dP^T = V dO_i^T                     (N = 128)
+//   WG0/1: P^T = exp2(S^T tau log2e - lse2), dS^T = P^T (dP^T - D), for
+//          query columns [64c, 64c + 64) each; P^T and dS^T go back into
+//          TMEM as 16-bit pairs and dS^T also into shared memory
+//   MMA:   dV += P^T dO_i, dK += dS^T Q_i (A from TMEM), dQ = dS K_j
+//   WG0/1: dQ rows read out of TMEM, staged in shared memory over the Q_i /
+//          dO_i tiles (no longer read by then); warp 2 adds them to dq_accum
+//          with TMA tensor reduce-adds and hands the stage back to the TMA
+//          producer.
+//
+// TMEM columns: S^T at 0 (then P^T at 0 and dS^T at 64, packed), dP^T at 128
+// (then dQ at 128, d columns), dV at 256, dK at 256 + d.  The next block's
+// S^T is issued right after dQ; its dP^T waits until dQ has been read out.
 template <int D>
 struct BwdCfg {
     static constexpr int STAGES = (D == 128) ? 2 : 3;       // Q_i / dO_i ring depth
@@ -314,16 +320,17 @@ struct BwdCfg {
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_DOFULL = B_QFULL + STAGES;
-    static constexpr int B_QEMPTY = B_DOFULL + STAGES;
+    static constexpr int B_QEMPTY = B_DOFULL + STAGES;      // stage free (after dQ reduce read)
     static constexpr int B_STFULL = B_QEMPTY + STAGES;      // stats ready  [S]
     static constexpr int B_STEMPTY = B_STFULL + STAGES;     // stats free   [S]
-    static constexpr int B_SDP = B_STEMPTY + STAGES;        // S^T and dP^T in TMEM
-    static constexpr int B_DS = B_SDP + 1;                  // P^T, dS^T written
+    static constexpr int B_SDP = B_STEMPTY + STAGES;        // S^T, dP^T in TMEM
+    static constexpr int B_LD = B_SDP + 1;                  // both warpgroups read S^T, dP^T
+    static constexpr int B_DS = B_LD + 1;                   // P^T, dS^T written
     static constexpr int B_DQFULL = B_DS + 1;               // dQ in TMEM
-    static constexpr int B_DQEMPTY = B_DQFULL + 1;          // dQ read out
-    static constexpr int B_ACC = B_DQEMPTY + 1;             // dV, dK final
-    static constexpr int B_LDDONE = B_ACC + 1;             // both warpgroups read S^T/dP^T
-    static constexpr int B_DRAIN = B_LDDONE + 1;
+    static constexpr int B_DQEMPTY = B_DQFULL + 1;          // dQ columns read out
+    static constexpr int B_STAGED = B_DQEMPTY + 1;          // dQ staged in smem
+    static constexpr int B_ACC = B_STAGED + 1;              // dV, dK final
+    static constexpr int B_DRAIN = B_ACC + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     // The d=128 layout needs (almost) all 227 KB, so it relies on the dynamic
@@ -332,16 +339,29 @@ struct BwdCfg {
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + SLACK;
     static constexpr int THREADS = 384;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
-    __device__ static constexpr uint32_t dq_col(int h) { return h == 0 ? 64u : 192u; }
+    static constexpr uint32_t S_COL = 0, P_COL = 0, DS_COL = 64, DP_COL = 128, DQ_COL = 128;
+    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+    static constexpr int DQ_BOX_COLS = 32;                  // fp32 columns per reduce box
+    static constexpr int DQ_BOX_BYTES = kTile * DQ_BOX_COLS * 4;   // 16 KB
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(D * kTile * 4 <= 2 * TILE_BYTES, "dQ staging fits in the Q_i + dO_i tiles");
 };
+
+// Staging address of dQ box b (fp32 columns [32b, 32b+32)) of stage s: boxes
+// fill the Q_i tile first, then the dO_i tile.
+template <int D>
+__device__ __forceinline__ uint32_t dq_box_addr(uint32_t sbase, int s, int b) {
+    using C = BwdCfg<D>;
+    constexpr int per_tile = C::TILE_BYTES / C::DQ_BOX_BYTES;   // 2 (d=128) or 1 (d=64)
+    return sbase + (b < per_tile ? C::Q_OFF : C::DO_OFF) + s * C::TILE_BYTES +
+           (b % per_tile) * C::DQ_BOX_BYTES;
+}
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdArgs args) {
+                const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -360,8 +380,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int j = blockIdx.y;                    // key block (causal: small j = most work)
+    const int bh = grid_head();
+    if (bh >= args.BH) return;                   // padding of the last grid z-slice
+    const int j = blockIdx.x;                    // key block (causal: small j = most work)
     const int N = args.N;
     const int nq = args.num_kvblocks;            // query blocks == key blocks
     const int i_start = CAUSAL ? j : 0;
@@ -377,14 +398,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(C::B_STEMPTY + s), 256);
         }
         mbar_init(bar(C::B_SDP), 1);
+        mbar_init(bar(C::B_LD), 256);
         mbar_init(bar(C::B_DS), 256);
         mbar_init(bar(C::B_DQFULL), 1);
         mbar_init(bar(C::B_DQEMPTY), 256);
+        mbar_init(bar(C::B_STAGED), 256);
         mbar_init(bar(C::B_ACC), 1);
-        mbar_init(bar(C::B_LDDONE), 256);
         mbar_init(bar(C::B_DRAIN), 1);
-        // A failure recorded earlier on this device turns later CTAs into
-        // no-ops until the host reads and clears the status word.
         *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
         fence_barrier_init();
     }
@@ -393,6 +413,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -453,17 +474,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
             constexpr uint32_t id_kk = idesc_f16(128, 128, fmt, 0, 0);  // K x Q^T, V x dO^T
             constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
-            constexpr uint32_t id_dq = idesc_f16(128, 64, fmt, 1, 1);   // dS x K (both MN-major)
+            constexpr uint32_t id_dq = idesc_f16(128, D, fmt, 1, 1);    // dS x K (both MN-major)
             bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1;
-                if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
-                if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
-                tc_fence_after();
                 const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
                 const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
-                // S^T = K Q^T
+                if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
+                tc_fence_after();
+                // S^T = K Q^T   (P^T and dS^T of the previous block were consumed by
+                // the dV / dK MMAs issued before this one)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -472,6 +493,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                            smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
                 }
                 if (!(ok = wait_bar(wc, bar(C::B_DOFULL + s), ph))) break;
+                // dP^T overwrites the previous block's dQ: wait for its readout
+                if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
                 tc_fence_after();
                 // dP^T = V dO^T
 #pragma unroll
@@ -484,34 +507,46 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_commit(bar(C::B_SDP));
                 if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
                 tc_fence_after();
-                // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ss(tmem + C::dq_col(h),
-                               smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
-                               smem_desc(sbase + C::K_OFF + h * kBoxBytes + kk * 2048, kBoxBytes, 1024,
-                                         LAYOUT_SW128),
-                               id_dq, kk > 0);
-                }
-                mma_commit(bar(C::B_DQFULL));
-                // dV += P^T dO ; dK += dS^T Q
+                // dV += P^T dO ; dK += dS^T Q   (K = the 128 queries of block i)
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8,
+                    mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8,
                            smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
                            (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8,
+                    mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8,
                            smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
                            (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(C::B_QEMPTY + s));
+                // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ss(tmem + C::DQ_COL,
+                           smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                           smem_desc(sbase + C::K_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                           id_dq, kk > 0);
+                mma_commit(bar(C::B_DQFULL));
             }
             if (ok) mma_commit(bar(C::B_ACC));
             mma_commit(bar(C::B_DRAIN));
             drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ dQ reducer
+        if (lane == 0) {
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::STAGES;
+                if (!wait_bar(wc, bar(C::B_STAGED), it & 1)) break;
+                fence_proxy_async_smem();
+#pragma unroll
+                for (int b = 0; b < D / C::DQ_BOX_COLS; ++b)
+                    tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
+                                      (i_start + it) * kTile, bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+                mbar_arrive(bar(C::B_QEMPTY + s));
+            }
+            bulk_wait_group0();
         }
     } else if (warp == 3) {
         // ------------------------------------------------------------ lse / D loader
@@ -530,12 +565,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int qi = q0 + lane * 4 + e;
                 const bool valid = qi < N;
                 // P = exp(tau s - lse) = exp2(tau log2e s - lse log2e); rows past N get P = 0
-                l2[lane * 4 + e] = valid ? lse_g[qi] * kLog2e : INFINITY;
+                l2[lane * 4 + e] = valid ? -lse_g[qi] * kLog2e : -INFINITY;
                 dv[lane * 4 + e] = valid ? d_g[qi] : 0.f;
             }
             mbar_arrive(bar(C::B_STFULL + s));
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ compute warpgroups
         const int c = (warp - 4) >> 2;           // query half handled by this warpgroup
         const int wq = warp & 3;
@@ -543,6 +578,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int key = j * kTile + r;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float cs = args.scale_log2;
+        const bool key_ok = key < N;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::STAGES;
@@ -557,77 +593,78 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
             tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
             tmem_ld_wait();
-            // both warpgroups have read their S^T / dP^T columns before either
-            // overwrites them (bounded wait instead of a named barrier)
-            mbar_arrive(bar(C::B_LDDONE));
-            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LDDONE), it & 1));
-            if (!ok) break;
-            const float* l2 = stats + s * 2 * kTile + 64 * c;
-            const float* dv = l2 + kTile;
+            tc_fence_before();
+            // P^T / dS^T overwrite S^T columns the other warpgroup reads: both must
+            // have loaded first
+            mbar_arrive(bar(C::B_LD));
+            const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
+            const float4* dvv = reinterpret_cast<const float4*>(stats + s * 2 * kTile + kTile + 64 * c);
             const int qbase = i * kTile + 64 * c;
-            const bool key_ok = key < N;
             const bool diag = CAUSAL && (i == j);
             uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
+            uint32_t pp[32], pd[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pp[16], pd[16];
+            for (int e4 = 0; e4 < 16; ++e4) {
+                const float4 nl = l2[e4];      // -lse * log2e of 4 queries (broadcast load)
+                const float4 dd = dvv[e4];     // D of 4 queries
+                const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
+                const float dda[4] = {dd.x, dd.y, dd.z, dd.w};
+                float pv[4], dsv[4];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int q = 32 * h + 2 * e + u;
-                        float p = ex2_approx(fmaf(__uint_as_float(sr[q]), cs, -l2[q]));
-                        if (!key_ok || (diag && qbase + q < key)) p = 0.f;
-                        pv[u] = p;
-                        dsv[u] = p * (__uint_as_float(dr[q]) - dv[q]);
-                    }
-                    pp[e] = pack2<BF16>(pv[0], pv[1]);
-                    pd[e] = pack2<BF16>(dsv[0], dsv[1]);
+                for (int u = 0; u < 4; ++u) {
+                    const int q = 4 * e4 + u;
+                    float p = ex2_approx(fmaf(__uint_as_float(sr[q]), cs, nla[u]));
+                    if (!key_ok || (diag && qbase + q < key)) p = 0.f;
+                    pv[u] = p;
+                    dsv[u] = p * (__uint_as_float(dr[q]) - dda[u]);
                 }
-                tmem_st16(tmem + lane_off + C::S_COL + 32 * c + 16 * h, pp);
-                tmem_st16(tmem + lane_off + C::DP_COL + 32 * c + 16 * h, pd);
-                // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of
-                // row r sits at chunk position k ^ (r % 8)
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int chunk = 4 * h + k4;
-                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
-                        make_uint4(pd[4 * k4], pd[4 * k4 + 1], pd[4 * k4 + 2], pd[4 * k4 + 3]);
-                }
+                pp[2 * e4] = pack2<BF16>(pv[0], pv[1]);
+                pp[2 * e4 + 1] = pack2<BF16>(pv[2], pv[3]);
+                pd[2 * e4] = pack2<BF16>(dsv[0], dsv[1]);
+                pd[2 * e4 + 1] = pack2<BF16>(dsv[2], dsv[3]);
             }
+            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LD), it & 1));
+            if (!ok) break;
+            tc_fence_after();
+            tmem_st32(tmem + lane_off + C::P_COL + 32 * c, pp);
+            tmem_st32(tmem + lane_off + C::DS_COL + 32 * c, pd);
+            // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of row
+            // r sits at chunk position k ^ (r % 8)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(ds_row + ((k ^ (r & 7)) * 16)) =
+                    make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(C::B_DS));
             mbar_arrive(bar(C::B_STEMPTY + s));
-            // dQ_i readout: lane = query row of block i
+            // dQ_i readout (lane = query row of block i) and staging for the reducer
             ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1));
             if (!ok) break;
             tc_fence_after();
-            const int qrow = i * kTile + r;
-            float* dq_row = args.dq_accum + (static_cast<size_t>(bh) * N + qrow) * D;
-            // Read this warpgroup's dQ columns out of TMEM, release the columns to
-            // the MMA issuer at once, then add them to dq_accum while the next
-            // tile's MMAs already run.
             constexpr int NQ = D / 2;                 // dQ columns per warpgroup
             uint32_t q32[NQ];
-            const uint32_t qcol = (D == 128) ? C::dq_col(c) : C::dq_col(0) + 32 * c;
 #pragma unroll
             for (int h = 0; h < NQ / 32; ++h)
-                tmem_ld32(tmem + lane_off + qcol + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
+                tmem_ld32(tmem + lane_off + C::DQ_COL + NQ * c + 32 * h,
+                          *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(bar(C::B_DQEMPTY));
-            if (qrow < N) {
-                float4* dst = reinterpret_cast<float4*>(dq_row + NQ * c);
+            // boxes of 32 fp32 columns, 128-byte swizzle: 16-byte chunk k of row r
+            // at chunk position k ^ (r % 8)
 #pragma unroll
-                for (int v4 = 0; v4 < NQ / 4; ++v4)
-                    atomicAdd(dst + v4, make_float4(__uint_as_float(q32[4 * v4]),
-                                                    __uint_as_float(q32[4 * v4 + 1]),
-                                                    __uint_as_float(q32[4 * v4 + 2]),
-                                                    __uint_as_float(q32[4 * v4 + 3])));
+            for (int h = 0; h < NQ / 32; ++h) {
+                uint8_t* box = smem + (dq_box_addr<D>(sbase, s, c * (NQ / 32) + h) - sbase) + r * 128;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(box + ((k ^ (r & 7)) * 16)) =
+                        make_uint4(q32[32 * h + 4 * k], q32[32 * h + 4 * k + 1],
+                                   q32[32 * h + 4 * k + 2], q32[32 * h + 4 * k + 3]);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(C::B_STAGED));
         }
         // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
@@ -691,15 +728,15 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
 
 template <int D, bool CAUSAL, bool BF16>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdArgs& a, int BH,
-                                cudaStream_t stream) {
+                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                                int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(BH, a.num_kvblocks);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    const dim3 grid = head_major_grid(a.num_kvblocks, BH);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaGetLastError();
 }
 
@@ -712,7 +749,7 @@ static cudaError_t launch_pre_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(BH, (a.N + kTile - 1) / kTile);
+    const dim3 grid = head_major_grid((a.N + kTile - 1) / kTile, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }
@@ -735,10 +772,10 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int BH, int d, bool causal,
-                       bool bf16, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int BH,
+                       int d, bool causal, bool bf16, cudaStream_t stream) {
 #define ATTN_BWD_CASE(D_, C_, B_) \
-    if (d == D_ && causal == C_ && bf16 == B_) return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, a, BH, stream);
+    if (d == D_ && causal == C_ && bf16 == B_) return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, tdq, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)
     ATTN_BWD_CASE(64, true, true)
     ATTN_BWD_CASE(128, false, true)

@@ -24,6 +24,7 @@ struct FwdArgs {
     float* lse;            // [B*H, N] fp32, written (natural log, scale inside)
     int* status;           // device status word
     int N;                 // sequence length
+    int BH;                // batch * heads
     int num_qblocks;       // ceil(N / 256): CTAs per head
     float scale_log2;      // softmax scale * log2(e)
     unsigned long long timeout_ns;
@@ -32,11 +33,12 @@ struct FwdArgs {
 struct BwdArgs {
     const float* lse;      // [B*H, N]
     const float* D;        // [B*H, N]
-    float* dq_accum;       // [B*H, N, d] fp32 (accumulated with reductions)
+    float* dq_accum;       // [B*H, N, d] fp32 (reduced into through a tensor map)
     void* dk;              // [B*H, N, d] 16-bit
     void* dv;              // [B*H, N, d] 16-bit
     int* status;
     int N;
+    int BH;                // batch * heads
     int num_kvblocks;      // ceil(N / 128)
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
@@ -49,6 +51,7 @@ struct DsumArgs {
     float* dq_accum;       // [B*H, N, d] fp32, zeroed
     int* status;
     int N;
+    int BH;                // batch * heads
     float scale_log2;      // tau * log2(e)
     unsigned long long timeout_ns;
 };
@@ -65,12 +68,27 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const FwdArgs& a, int BH, int d, bool causal, bool bf16,
                        cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int BH, int d, bool causal,
-                       bool bf16, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int BH,
+                       int d, bool causal, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const DsumArgs& a, int BH, int d, bool causal,
                             bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
+
+// Grid layout shared by the attention kernels: x = block index within a head
+// (mapped so that the heaviest causal blocks start first), y/z = (batch, head)
+// so that the CTAs resident at one time belong to a few heads and share their
+// K/V (forward, preprocess) or Q/dO (backward) tiles in L2.
+constexpr int kMaxGridY = 65535;
+
+inline dim3 head_major_grid(int blocks_per_head, int BH) {
+    const int gy = BH < kMaxGridY ? BH : kMaxGridY;
+    return dim3(blocks_per_head, gy, (BH + gy - 1) / gy);
+}
+
+__device__ __forceinline__ int grid_head() {
+    return static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &

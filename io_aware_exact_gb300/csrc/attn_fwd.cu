@@ -78,8 +78,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int qb = args.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // heavy blocks first
+    const int bh = grid_head();
+    if (bh >= args.BH) return;                   // padding of the last grid z-slice
+    const int qb = args.num_qblocks - 1 - static_cast<int>(blockIdx.x);  // heavy blocks first
     const int q0 = qb * (C::TILES * kTile);
     const int N = args.N;
     const int nkv_all = (N + kTile - 1) / kTile;
@@ -359,7 +360,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(BH, a.num_qblocks);
+    const dim3 grid = head_major_grid(a.num_qblocks, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
