@@ -105,6 +105,23 @@ def _dist():
     return world, rank, local
 
 
+def dist_max(value: float, device="cpu") -> float:
+    """Maximum of `value` over all ranks (the value itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, max_ms: float) -> float:
+    """Units per second of the whole job: every rank processes `units_per_rank`
+    (weak scaling); the job takes as long as its slowest rank."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
 def run_ours(args):
     import torch
     import io_aware_exact_gb300 as attn
@@ -172,12 +189,7 @@ def run_ours(args):
     t_fwd = [e[0].elapsed_time(e[1]) for e in evs]
     t_pre = [e[1].elapsed_time(e[2]) for e in evs]
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
-    ms_step = sum(t_step) / len(t_step)
-    if pg:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = dist_max(sum(t_step) / len(t_step), dev)
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = None
@@ -213,7 +225,7 @@ def run_ours(args):
 
     peaks = _peaks()
     flops_fb = w.flops_fwd_bwd()
-    tflops_fb = world * flops_fb / (ms_step * 1e-3) / 1e12
+    tflops_fb = whole_job_rate(world, flops_fb, ms_step) / 1e12
     ms_fwd = statistics.mean(t_fwd)
     ms_bwd = statistics.mean(t_bwd)
     tflops_fwd = w.flops_fwd() / (ms_fwd * 1e-3) / 1e12
@@ -223,13 +235,7 @@ def run_ours(args):
     bwd_tflops = flops_bwd_kernel / (ms_bwd * 1e-3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            tr = json.load(f)
-        if tr.get("workload") == args.workload and tr.get("kernel_rev") == KERNEL_REV:
-            traffic = tr.get("bytes_per_launch")
+    traffic = profile_traffic(args.workload)
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -272,7 +278,38 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-KERNEL_REV = "bwd-v1"
+BWD_PROFILE = os.path.join(ROOT, "profiles", "attn_bwd_kernel_causal_b2_h16_n8192_d128.md")
+BWD_SOURCES = [os.path.join(ROOT, "io_aware_exact_gb300", "csrc", f)
+               for f in ("attn_bwd.cu", "attn_common.cuh", "ptx.cuh")]
+
+
+def kernel_source_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for p in BWD_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profile_traffic(workload):
+    """DRAM bytes per launch of the backward main kernel from the committed ncu
+    summary, or None if there is none for this workload or the kernel's source
+    changed since it was captured."""
+    if workload != HEADLINE or not os.path.exists(BWD_PROFILE):
+        return None
+    fields = {}
+    with open(BWD_PROFILE) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256") != kernel_source_sha256():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def _oracle_step(w, x, heads):

@@ -104,11 +104,11 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = grid_head();
-    if (bh >= args.BH) return;                   // padding of the last grid z-slice
+    const int bh = blockIdx.x;
     const int N = args.N;
     const int nblk = (N + kTile - 1) / kTile;
-    const int qi = nblk - 1 - static_cast<int>(blockIdx.x);     // heavy query blocks first
+    if (grid_block() >= nblk) return;                               // padding CTA
+    const int qi = nblk - 1 - grid_block();                         // heavy query blocks first
     const int nkv = CAUSAL ? min(nblk, qi + 1) : nblk;
 
     if (threadIdx.x == 0) {
@@ -238,7 +238,7 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float cs = args.scale_log2;
         const float nl2 = (row < N) ? -args.lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
-        float acc0 = 0.f, acc1 = 0.f;
+        uint64_t acc2 = f2_pack(0.f, 0.f);
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
             const int b = j & 1;
@@ -248,25 +248,44 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // keys >= limit are masked: the key tail and, on the diagonal block, keys > row
             int limit = N - (j * kTile + 64 * c);
             if (CAUSAL) limit = min(limit, row - (j * kTile + 64 * c) + 1);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c + 32 * h, sr);
-                tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c + 32 * h, dr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), cs, nl2));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), cs, nl2));
-                    if (32 * h + e >= limit) p0 = 0.f;
-                    if (32 * h + e + 1 >= limit) p1 = 0.f;
-                    acc0 = fmaf(p0, __uint_as_float(dr[e]), acc0);
-                    acc1 = fmaf(p1, __uint_as_float(dr[e + 1]), acc1);
-                }
-            }
+            // all four loads in flight before one wait
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+            tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+            tmem_ld_wait();
+            // the buffer can be refilled as soon as it has been read
             tc_fence_before();
             mbar_arrive(bar(C::B_FREE + b));
+            const uint64_t cs2 = f2_pack(cs, cs);
+            const uint64_t nl22 = f2_pack(nl2, nl2);
+            if (limit >= 64) {
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const uint64_t arg = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                cs2, nl22);
+                    float a0, a1;
+                    f2_unpack(arg, a0, a1);
+                    acc2 = f2_fma(f2_pack(ex2_approx(a0), ex2_approx(a1)),
+                                  f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), acc2);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const uint64_t arg = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                cs2, nl22);
+                    float a0, a1;
+                    f2_unpack(arg, a0, a1);
+                    const float p0 = (e >= limit) ? 0.f : ex2_approx(a0);
+                    const float p1 = (e + 1 >= limit) ? 0.f : ex2_approx(a1);
+                    acc2 = f2_fma(f2_pack(p0, p1),
+                                  f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), acc2);
+                }
+            }
         }
+        float acc0, acc1;
+        f2_unpack(acc2, acc0, acc1);
         const float acc = acc0 + acc1;
         if (c == 1) {
             red[r] = acc;
@@ -380,9 +399,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = grid_head();
-    if (bh >= args.BH) return;                   // padding of the last grid z-slice
-    const int j = blockIdx.x;                    // key block (causal: small j = most work)
+    const int bh = blockIdx.x;
+    if (grid_block() >= args.num_kvblocks) return;                  // padding CTA
+    const int j = grid_block();                  // key block (causal: small j = most work)
     const int N = args.N;
     const int nq = args.num_kvblocks;            // query blocks == key blocks
     const int i_start = CAUSAL ? j : 0;
@@ -426,271 +445,300 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
     const bool skip = *abort_flag != 0;
 
-    if (skip) {
-        // nothing issued, nothing to drain
-    } else if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_kv = policy_evict_first();
-            const uint64_t pol_q = policy_evict_last();
-            mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
-            for (int b = 0; b < C::KBOX; ++b) {
-                tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
-                            j * kTile, bh, pol_kv);
-                tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
-                            j * kTile, bh, pol_kv);
-            }
-            int issued = 0;
-            bool ok = true;
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % C::STAGES;
-                const int i = i_start + it;
-                if (it >= C::STAGES) {
-                    ok = wait_bar(wc, bar(C::B_QEMPTY + s), ((it / C::STAGES) - 1) & 1);
-                    if (!ok) break;
+    // Register budgets: 384 threads x 168 registers at launch; the role warps
+    // (TMA, MMA, dQ reducer, lse/D loader) need few, the two compute
+    // warpgroups many: 128 x 120 + 256 x 192 = 384 x 168.
+    static_assert(C::THREADS * 168 == 128 * 120 + 256 * 192, "register split");
+    if (warp < 4) {
+        regs_dec<120>();
+        if (!skip) {
+            if (warp == 0) {
+                // ------------------------------------------------------------ TMA producer
+                if (lane == 0) {
+                    const uint64_t pol_kv = policy_evict_first();
+                    const uint64_t pol_q = policy_evict_last();
+                    mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
+                    for (int b = 0; b < C::KBOX; ++b) {
+                        tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
+                                    j * kTile, bh, pol_kv);
+                        tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
+                                    j * kTile, bh, pol_kv);
+                    }
+                    int issued = 0;
+                    bool ok = true;
+                    for (int it = 0; it < n_it; ++it) {
+                        const int s = it % C::STAGES;
+                        const int i = i_start + it;
+                        if (it >= C::STAGES) {
+                            ok = wait_bar(wc, bar(C::B_QEMPTY + s), ((it / C::STAGES) - 1) & 1);
+                            if (!ok) break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
+                        for (int b = 0; b < C::KBOX; ++b)
+                            tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                        bar(C::B_QFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
+                        mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
+                        for (int b = 0; b < C::KBOX; ++b)
+                            tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
+                                        bar(C::B_DOFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
+                        issued = it + 1;
+                    }
+                    if (!ok) {
+                        drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
+                        for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+                            const int s = it % C::STAGES;
+                            drain_wait(bar(C::B_QFULL + s), (it / C::STAGES) & 1, 1000000000ull);
+                            drain_wait(bar(C::B_DOFULL + s), (it / C::STAGES) & 1, 1000000000ull);
+                        }
+                    }
                 }
-                mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
-                for (int b = 0; b < C::KBOX; ++b)
-                    tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                bar(C::B_QFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
-                mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
-                for (int b = 0; b < C::KBOX; ++b)
-                    tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
-                                bar(C::B_DOFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
-                issued = it + 1;
-            }
-            if (!ok) {
-                drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
-                for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+            } else if (warp == 1) {
+                // ------------------------------------------------------------ MMA issuer
+                if (lane == 0) {
+                    constexpr uint32_t fmt = BF16 ? 1u : 0u;
+                    constexpr uint32_t id_kk = idesc_f16(128, 128, fmt, 0, 0);  // K x Q^T, V x dO^T
+                    constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
+                    constexpr uint32_t id_dq = idesc_f16(128, D, fmt, 1, 1);    // dS x K (both MN-major)
+                    bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
+                    for (int it = 0; ok && it < n_it; ++it) {
+                        const int s = it % C::STAGES;
+                        const uint32_t ph = (it / C::STAGES) & 1;
+                        const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
+                        const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
+                        if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
+                        tc_fence_after();
+                        // S^T = K Q^T   (P^T and dS^T of the previous block were consumed by
+                        // the dV / dK MMAs issued before this one)
+        #pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                            mma_ss(tmem + C::S_COL,
+                                   smem_desc(sbase + C::K_OFF + off, 16, 1024, LAYOUT_SW128),
+                                   smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                        }
+                        if (!(ok = wait_bar(wc, bar(C::B_DOFULL + s), ph))) break;
+                        // dP^T overwrites the previous block's dQ: wait for its readout
+                        if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
+                        tc_fence_after();
+                        // dP^T = V dO^T
+        #pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                            mma_ss(tmem + C::DP_COL,
+                                   smem_desc(sbase + C::V_OFF + off, 16, 1024, LAYOUT_SW128),
+                                   smem_desc(do_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                        }
+                        mma_commit(bar(C::B_SDP));
+                        if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
+                        tc_fence_after();
+                        // dV += P^T dO ; dK += dS^T Q   (K = the 128 queries of block i)
+        #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8,
+                                   smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
+                                   (it > 0 || kk > 0) ? 1u : 0u);
+        #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8,
+                                   smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
+                                   (it > 0 || kk > 0) ? 1u : 0u);
+                        // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
+        #pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem + C::DQ_COL,
+                                   smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                                   smem_desc(sbase + C::K_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                                   id_dq, kk > 0);
+                        mma_commit(bar(C::B_DQFULL));
+                    }
+                    if (ok) mma_commit(bar(C::B_ACC));
+                    mma_commit(bar(C::B_DRAIN));
+                    drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+                }
+            } else if (warp == 2) {
+                // ------------------------------------------------------------ dQ reducer
+                if (lane == 0) {
+                    for (int it = 0; it < n_it; ++it) {
+                        const int s = it % C::STAGES;
+                        if (!wait_bar(wc, bar(C::B_STAGED), it & 1)) break;
+                        fence_proxy_async_smem();
+        #pragma unroll
+                        for (int b = 0; b < D / C::DQ_BOX_COLS; ++b)
+                            tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
+                                              (i_start + it) * kTile, bh);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();
+                        mbar_arrive(bar(C::B_QEMPTY + s));
+                    }
+                    bulk_wait_group0();
+                }
+            } else if (warp == 3) {
+                // ------------------------------------------------------------ lse / D loader
+                const float* lse_g = args.lse + static_cast<size_t>(bh) * N;
+                const float* d_g = args.D + static_cast<size_t>(bh) * N;
+                for (int it = 0; it < n_it; ++it) {
                     const int s = it % C::STAGES;
-                    drain_wait(bar(C::B_QFULL + s), (it / C::STAGES) & 1, 1000000000ull);
-                    drain_wait(bar(C::B_DOFULL + s), (it / C::STAGES) & 1, 1000000000ull);
+                    if (it >= C::STAGES &&
+                        !__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_STEMPTY + s), ((it / C::STAGES) - 1) & 1)))
+                        break;
+                    const int q0 = (i_start + it) * kTile;
+                    float* l2 = stats + s * 2 * kTile;
+                    float* dv = l2 + kTile;
+        #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int qi = q0 + lane * 4 + e;
+                        const bool valid = qi < N;
+                        // P = exp(tau s - lse) = exp2(tau log2e s - lse log2e); rows past N get P = 0
+                        l2[lane * 4 + e] = valid ? -lse_g[qi] * kLog2e : -INFINITY;
+                        dv[lane * 4 + e] = valid ? -d_g[qi] : 0.f;
+                    }
+                    mbar_arrive(bar(C::B_STFULL + s));
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t fmt = BF16 ? 1u : 0u;
-            constexpr uint32_t id_kk = idesc_f16(128, 128, fmt, 0, 0);  // K x Q^T, V x dO^T
-            constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
-            constexpr uint32_t id_dq = idesc_f16(128, D, fmt, 1, 1);    // dS x K (both MN-major)
-            bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1;
-                const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
-                const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
-                if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
-                tc_fence_after();
-                // S^T = K Q^T   (P^T and dS^T of the previous block were consumed by
-                // the dV / dK MMAs issued before this one)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::S_COL,
-                           smem_desc(sbase + C::K_OFF + off, 16, 1024, LAYOUT_SW128),
-                           smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
-                }
-                if (!(ok = wait_bar(wc, bar(C::B_DOFULL + s), ph))) break;
-                // dP^T overwrites the previous block's dQ: wait for its readout
-                if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
-                tc_fence_after();
-                // dP^T = V dO^T
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::DP_COL,
-                           smem_desc(sbase + C::V_OFF + off, 16, 1024, LAYOUT_SW128),
-                           smem_desc(do_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
-                }
-                mma_commit(bar(C::B_SDP));
-                if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
-                tc_fence_after();
-                // dV += P^T dO ; dK += dS^T Q   (K = the 128 queries of block i)
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8,
-                           smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8,
-                           smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-                // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ss(tmem + C::DQ_COL,
-                           smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
-                           smem_desc(sbase + C::K_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
-                           id_dq, kk > 0);
-                mma_commit(bar(C::B_DQFULL));
-            }
-            if (ok) mma_commit(bar(C::B_ACC));
-            mma_commit(bar(C::B_DRAIN));
-            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ dQ reducer
-        if (lane == 0) {
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % C::STAGES;
-                if (!wait_bar(wc, bar(C::B_STAGED), it & 1)) break;
-                fence_proxy_async_smem();
-#pragma unroll
-                for (int b = 0; b < D / C::DQ_BOX_COLS; ++b)
-                    tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
-                                      (i_start + it) * kTile, bh);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-                mbar_arrive(bar(C::B_QEMPTY + s));
-            }
-            bulk_wait_group0();
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ lse / D loader
-        const float* lse_g = args.lse + static_cast<size_t>(bh) * N;
-        const float* d_g = args.D + static_cast<size_t>(bh) * N;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % C::STAGES;
-            if (it >= C::STAGES &&
-                !__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_STEMPTY + s), ((it / C::STAGES) - 1) & 1)))
-                break;
-            const int q0 = (i_start + it) * kTile;
-            float* l2 = stats + s * 2 * kTile;
-            float* dv = l2 + kTile;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int qi = q0 + lane * 4 + e;
-                const bool valid = qi < N;
-                // P = exp(tau s - lse) = exp2(tau log2e s - lse log2e); rows past N get P = 0
-                l2[lane * 4 + e] = valid ? -lse_g[qi] * kLog2e : -INFINITY;
-                dv[lane * 4 + e] = valid ? d_g[qi] : 0.f;
-            }
-            mbar_arrive(bar(C::B_STFULL + s));
         }
     } else {
-        // ------------------------------------------------------------ compute warpgroups
-        const int c = (warp - 4) >> 2;           // query half handled by this warpgroup
-        const int wq = warp & 3;
-        const int r = wq * 32 + lane;            // TMEM lane: key row (and query row for dQ)
-        const int key = j * kTile + r;
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const float cs = args.scale_log2;
-        const bool key_ok = key < N;
-        bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % C::STAGES;
-            const int i = i_start + it;
-            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SDP), it & 1) &&
-                                             wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[64], dr[64];
-            tmem_ld32(tmem + lane_off + C::S_COL + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(tmem + lane_off + C::S_COL + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-            tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            // P^T / dS^T overwrite S^T columns the other warpgroup reads: both must
-            // have loaded first
-            mbar_arrive(bar(C::B_LD));
-            const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
-            const float4* dvv = reinterpret_cast<const float4*>(stats + s * 2 * kTile + kTile + 64 * c);
-            const int qbase = i * kTile + 64 * c;
-            const bool diag = CAUSAL && (i == j);
-            uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
-            uint32_t pp[32], pd[32];
-#pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
-                const float4 nl = l2[e4];      // -lse * log2e of 4 queries (broadcast load)
-                const float4 dd = dvv[e4];     // D of 4 queries
-                const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
-                const float dda[4] = {dd.x, dd.y, dd.z, dd.w};
-                float pv[4], dsv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int q = 4 * e4 + u;
-                    float p = ex2_approx(fmaf(__uint_as_float(sr[q]), cs, nla[u]));
-                    if (!key_ok || (diag && qbase + q < key)) p = 0.f;
-                    pv[u] = p;
-                    dsv[u] = p * (__uint_as_float(dr[q]) - dda[u]);
+        regs_inc<192>();
+        if (!skip) {
+                // ------------------------------------------------------------ compute warpgroups
+                const int c = (warp - 4) >> 2;           // query half handled by this warpgroup
+                const int wq = warp & 3;
+                const int r = wq * 32 + lane;            // TMEM lane: key row (and query row for dQ)
+                const int key = j * kTile + r;
+                const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+                const float cs = args.scale_log2;
+                const bool key_ok = key < N;
+                bool ok = true;
+                for (int it = 0; it < n_it; ++it) {
+                    const int s = it % C::STAGES;
+                    const int i = i_start + it;
+                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SDP), it & 1) &&
+                                                     wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    // per query: -lse*log2e and -D (the loader stores both negated)
+                    const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
+                    const float4* dvv = reinterpret_cast<const float4*>(stats + s * 2 * kTile + kTile + 64 * c);
+                    const int qbase = i * kTile + 64 * c;
+                    // masking is needed only for keys past N and on the diagonal block
+                    const bool masked = !key_ok || (CAUSAL && i == j);
+                    uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
+                    const uint64_t cs2 = f2_pack(cs, cs);
+                    uint32_t pp[32], pd[32];
+                    // two chunks of 32 query columns keep ~64 inputs live instead of 128
+        #pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        // masked columns of this chunk are those below lim (the query
+                        // precedes the key; all of them past the key tail)
+                        const int lim = key_ok ? key - (qbase + 32 * ch) : 32;
+                        uint32_t sr[32], dr[32];
+                        tmem_ld32(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
+                        tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32 * ch, dr);
+                        tmem_ld_wait();
+                        if (ch == 1) {
+                            // P^T / dS^T overwrite S^T columns the other warpgroup reads:
+                            // both must have loaded them first
+                            tc_fence_before();
+                            mbar_arrive(bar(C::B_LD));
+                        }
+        #pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 nl = l2[8 * ch + e4];      // broadcast loads
+                            const float4 nd = dvv[8 * ch + e4];
+                            const uint64_t nl2[2] = {f2_pack(nl.x, nl.y), f2_pack(nl.z, nl.w)};
+                            const uint64_t nd2[2] = {f2_pack(nd.x, nd.y), f2_pack(nd.z, nd.w)};
+        #pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int q = 4 * e4 + 2 * u;        // column within the chunk
+                                // P = exp2(s tau log2e - lse log2e), two queries per instruction
+                                const uint64_t arg = f2_fma(f2_pack(__uint_as_float(sr[q]), __uint_as_float(sr[q + 1])),
+                                                            cs2, nl2[u]);
+                                float a0, a1;
+                                f2_unpack(arg, a0, a1);
+                                float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                                if (masked) {
+                                    if (q < lim) p0 = 0.f;
+                                    if (q + 1 < lim) p1 = 0.f;
+                                }
+                                // dS = P (dP - D)
+                                const uint64_t dsv = f2_mul(f2_pack(p0, p1),
+                                                            f2_add(f2_pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1])),
+                                                                   nd2[u]));
+                                float d0, d1;
+                                f2_unpack(dsv, d0, d1);
+                                pp[16 * ch + 2 * e4 + u] = pack2<BF16>(p0, p1);
+                                pd[16 * ch + 2 * e4 + u] = pack2<BF16>(d0, d1);
+                            }
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LD), it & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    tmem_st32(tmem + lane_off + C::P_COL + 32 * c, pp);
+                    tmem_st32(tmem + lane_off + C::DS_COL + 32 * c, pd);
+                    // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of row
+                    // r sits at chunk position k ^ (r % 8)
+        #pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4*>(ds_row + ((k ^ (r & 7)) * 16)) =
+                            make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
+                    tmem_st_wait();
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_DS));
+                    mbar_arrive(bar(C::B_STEMPTY + s));
+                    // dQ_i readout (lane = query row of block i) and staging for the reducer
+                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    constexpr int NQ = D / 2;                 // dQ columns per warpgroup
+                    uint32_t q32[NQ];
+        #pragma unroll
+                    for (int h = 0; h < NQ / 32; ++h)
+                        tmem_ld32(tmem + lane_off + C::DQ_COL + NQ * c + 32 * h,
+                                  *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_DQEMPTY));
+                    // boxes of 32 fp32 columns, 128-byte swizzle: 16-byte chunk k of row r
+                    // at chunk position k ^ (r % 8)
+        #pragma unroll
+                    for (int h = 0; h < NQ / 32; ++h) {
+                        uint8_t* box = smem + (dq_box_addr<D>(sbase, s, c * (NQ / 32) + h) - sbase) + r * 128;
+        #pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4*>(box + ((k ^ (r & 7)) * 16)) =
+                                make_uint4(q32[32 * h + 4 * k], q32[32 * h + 4 * k + 1],
+                                           q32[32 * h + 4 * k + 2], q32[32 * h + 4 * k + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::B_STAGED));
                 }
-                pp[2 * e4] = pack2<BF16>(pv[0], pv[1]);
-                pp[2 * e4 + 1] = pack2<BF16>(pv[2], pv[3]);
-                pd[2 * e4] = pack2<BF16>(dsv[0], dsv[1]);
-                pd[2 * e4 + 1] = pack2<BF16>(dsv[2], dsv[3]);
-            }
-            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LD), it & 1));
-            if (!ok) break;
-            tc_fence_after();
-            tmem_st32(tmem + lane_off + C::P_COL + 32 * c, pp);
-            tmem_st32(tmem + lane_off + C::DS_COL + 32 * c, pd);
-            // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of row
-            // r sits at chunk position k ^ (r % 8)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                *reinterpret_cast<uint4*>(ds_row + ((k ^ (r & 7)) * 16)) =
-                    make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
-            tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_DS));
-            mbar_arrive(bar(C::B_STEMPTY + s));
-            // dQ_i readout (lane = query row of block i) and staging for the reducer
-            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1));
-            if (!ok) break;
-            tc_fence_after();
-            constexpr int NQ = D / 2;                 // dQ columns per warpgroup
-            uint32_t q32[NQ];
-#pragma unroll
-            for (int h = 0; h < NQ / 32; ++h)
-                tmem_ld32(tmem + lane_off + C::DQ_COL + NQ * c + 32 * h,
-                          *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_DQEMPTY));
-            // boxes of 32 fp32 columns, 128-byte swizzle: 16-byte chunk k of row r
-            // at chunk position k ^ (r % 8)
-#pragma unroll
-            for (int h = 0; h < NQ / 32; ++h) {
-                uint8_t* box = smem + (dq_box_addr<D>(sbase, s, c * (NQ / 32) + h) - sbase) + r * 128;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    *reinterpret_cast<uint4*>(box + ((k ^ (r & 7)) * 16)) =
-                        make_uint4(q32[32 * h + 4 * k], q32[32 * h + 4 * k + 1],
-                                   q32[32 * h + 4 * k + 2], q32[32 * h + 4 * k + 3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(C::B_STAGED));
-        }
-        // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
-        if (ok) {
-            tc_fence_after();
-            const float mul = (c == 0) ? 1.0f : args.scale;
-            const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
-            uint16_t* out = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
-                            (static_cast<size_t>(bh) * N + key) * D;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-                uint32_t a32[32];
-                tmem_ld32(tmem + lane_off + col + cc, a32);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2<BF16>(__uint_as_float(a32[2 * e]) * mul,
-                                        __uint_as_float(a32[2 * e + 1]) * mul);
-                if (key < N) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + cc);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
+                if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
+                if (ok) {
+                    tc_fence_after();
+                    const float mul = (c == 0) ? 1.0f : args.scale;
+                    const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
+                    uint16_t* out = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
+                                    (static_cast<size_t>(bh) * N + key) * D;
+        #pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t a32[32];
+                        tmem_ld32(tmem + lane_off + col + cc, a32);
+                        tmem_ld_wait();
+                        uint32_t pk[16];
+        #pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack2<BF16>(__uint_as_float(a32[2 * e]) * mul,
+                                                __uint_as_float(a32[2 * e + 1]) * mul);
+                        if (key < N) {
+                            uint4* dst = reinterpret_cast<uint4*>(out + cc);
+        #pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
+                    }
                 }
-            }
         }
     }
 
@@ -735,7 +783,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const dim3 grid = head_major_grid(a.num_kvblocks, BH);
+    const dim3 grid = lpt_grid(a.num_kvblocks, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaGetLastError();
 }
@@ -749,7 +797,7 @@ static cudaError_t launch_pre_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const dim3 grid = head_major_grid((a.N + kTile - 1) / kTile, BH);
+    const dim3 grid = lpt_grid((a.N + kTile - 1) / kTile, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }

@@ -75,18 +75,21 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
                             bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
 
-// Grid layout shared by the attention kernels: x = block index within a head
-// (mapped so that the heaviest causal blocks start first), y/z = (batch, head)
-// so that the CTAs resident at one time belong to a few heads and share their
-// K/V (forward, preprocess) or Q/dO (backward) tiles in L2.
+// Grid layout shared by the attention kernels: x = (batch, head), y/z = block
+// index within a head.  Launch order is x fastest, so every head's heaviest
+// causal block is scheduled before any lighter one (longest work first; a
+// head-major order, tried as well, left a tail of heavy blocks of the last
+// heads).  y is capped at the hardware limit and z extends it.
 constexpr int kMaxGridY = 65535;
 
-inline dim3 head_major_grid(int blocks_per_head, int BH) {
-    const int gy = BH < kMaxGridY ? BH : kMaxGridY;
-    return dim3(blocks_per_head, gy, (BH + gy - 1) / gy);
+inline dim3 lpt_grid(int blocks_per_head, int BH) {
+    const int gy = blocks_per_head < kMaxGridY ? blocks_per_head : kMaxGridY;
+    return dim3(BH, gy, (blocks_per_head + gy - 1) / gy);
 }
 
-__device__ __forceinline__ int grid_head() {
+// Block index within the head (0 = first launched); >= blocks_per_head only
+// for padding CTAs of the last z-slice.
+__device__ __forceinline__ int grid_block() {
     return static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
 }
 

@@ -78,9 +78,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = grid_head();
-    if (bh >= args.BH) return;                   // padding of the last grid z-slice
-    const int qb = args.num_qblocks - 1 - static_cast<int>(blockIdx.x);  // heavy blocks first
+    const int bh = blockIdx.x;
+    if (grid_block() >= args.num_qblocks) return;                  // padding CTA
+    const int qb = args.num_qblocks - 1 - grid_block();            // heavy blocks first
     const int q0 = qb * (C::TILES * kTile);
     const int N = args.N;
     const int nkv_all = (N + kTile - 1) / kTile;
@@ -126,220 +126,233 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
     const bool skip = *abort_flag != 0;
 
-    if (skip) {
-        // nothing issued, nothing to drain
-    } else if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_q = policy_evict_first();
-            const uint64_t pol_kv = policy_evict_last();
-            const int ntiles = (nkv[1] > 0) ? 2 : 1;
-            mbar_arrive_expect_tx(bar(C::B_QFULL), ntiles * C::TILE_BYTES);
-            for (int t = 0; t < ntiles; ++t)
-                for (int b = 0; b < C::KBOX; ++b)
-                    tma_load_3d(sbase + C::Q_OFF + t * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                bar(C::B_QFULL), b * kBoxCols, q0 + kTile * t, bh, pol_q);
-            int issued = 0;
-            bool ok = true;
-            for (int j = 0; j < n_iter; ++j) {
-                const int s = j % C::STAGES;
-                if (j >= C::STAGES) {
-                    ok = wait_bar(wc, bar(C::B_KVEMPTY + s), ((j / C::STAGES) - 1) & 1);
-                    if (!ok) break;
-                }
-                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
-                for (int b = 0; b < C::KBOX; ++b)
-                    tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
-                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
-                for (int b = 0; b < C::KBOX; ++b)
-                    tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
-                issued = j + 1;
-            }
-            if (!ok) {
-                // let copies already in flight land before the CTA's smem goes away
-                drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
-                for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-                    drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
-                    drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t fmt = BF16 ? 1u : 0u;
-            constexpr uint32_t idesc_s = idesc_f16(128, 128, fmt, 0, 0);  // Q (K-major) x K (K-major)
-            constexpr uint32_t idesc_o = idesc_f16(128, D, fmt, 0, 1);    // P (TMEM) x V (MN-major)
-            auto issue_s = [&](int t, int s) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    const uint64_t a = smem_desc(sbase + C::Q_OFF + t * C::TILE_BYTES + off, 16,
-                                                 1024, LAYOUT_SW128);
-                    const uint64_t b = smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES + off, 16,
-                                                 1024, LAYOUT_SW128);
-                    mma_ss(tmem + C::s_col(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int s, bool acc) {
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t b = smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES + kk * 2048,
-                                                 kBoxBytes, 1024, LAYOUT_SW128);
-                    mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, b, idesc_o,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = wait_bar(wc, bar(C::B_QFULL), 0) && wait_bar(wc, bar(C::B_KFULL + 0), 0);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (nkv[t] > 0) {
-                        issue_s(t, 0);
-                        mma_commit(bar(C::B_SFULL + t));
+    if (warp < 4) {
+        if (skip) {
+            // nothing issued, nothing to drain
+        } else if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                const uint64_t pol_q = policy_evict_first();
+                const uint64_t pol_kv = policy_evict_last();
+                const int ntiles = (nkv[1] > 0) ? 2 : 1;
+                mbar_arrive_expect_tx(bar(C::B_QFULL), ntiles * C::TILE_BYTES);
+                for (int t = 0; t < ntiles; ++t)
+                    for (int b = 0; b < C::KBOX; ++b)
+                        tma_load_3d(sbase + C::Q_OFF + t * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                    bar(C::B_QFULL), b * kBoxCols, q0 + kTile * t, bh, pol_q);
+                int issued = 0;
+                bool ok = true;
+                for (int j = 0; j < n_iter; ++j) {
+                    const int s = j % C::STAGES;
+                    if (j >= C::STAGES) {
+                        ok = wait_bar(wc, bar(C::B_KVEMPTY + s), ((j / C::STAGES) - 1) & 1);
+                        if (!ok) break;
                     }
+                    mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
+                    for (int b = 0; b < C::KBOX; ++b)
+                        tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
+                                    bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                    mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
+                    for (int b = 0; b < C::KBOX; ++b)
+                        tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
+                                    bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                    issued = j + 1;
+                }
+                if (!ok) {
+                    // let copies already in flight land before the CTA's smem goes away
+                    drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
+                    for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+                        drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                        drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                    }
+                }
             }
-            for (int j = 0; ok && j < n_iter; ++j) {
-                const int s = j % C::STAGES;
-                if (!(ok = wait_bar(wc, bar(C::B_VFULL + s), (j / C::STAGES) & 1))) break;
-                bool next_k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nkv[t]) continue;
-                    if (!(ok = wait_bar(wc, bar(C::B_PFULL + t), j & 1))) break;
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t fmt = BF16 ? 1u : 0u;
+                constexpr uint32_t idesc_s = idesc_f16(128, 128, fmt, 0, 0);  // Q (K-major) x K (K-major)
+                constexpr uint32_t idesc_o = idesc_f16(128, D, fmt, 0, 1);    // P (TMEM) x V (MN-major)
+                auto issue_s = [&](int t, int s) {
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                        const uint64_t a = smem_desc(sbase + C::Q_OFF + t * C::TILE_BYTES + off, 16,
+                                                     1024, LAYOUT_SW128);
+                        const uint64_t b = smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES + off, 16,
+                                                     1024, LAYOUT_SW128);
+                        mma_ss(tmem + C::s_col(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](int t, int s, bool acc) {
+    #pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t b = smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES + kk * 2048,
+                                                     kBoxBytes, 1024, LAYOUT_SW128);
+                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, b, idesc_o,
+                               (acc || kk > 0) ? 1u : 0u);
+                    }
+                };
+                bool ok = wait_bar(wc, bar(C::B_QFULL), 0) && wait_bar(wc, bar(C::B_KFULL + 0), 0);
+                if (ok) {
                     tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    if (j + 1 < nkv[t]) {
-                        if (!next_k_ready) {
-                            const int s1 = (j + 1) % C::STAGES;
-                            if (!(ok = wait_bar(wc, bar(C::B_KFULL + s1), ((j + 1) / C::STAGES) & 1)))
-                                break;
-                            tc_fence_after();
-                            next_k_ready = true;
+                    for (int t = 0; t < 2; ++t)
+                        if (nkv[t] > 0) {
+                            issue_s(t, 0);
+                            mma_commit(bar(C::B_SFULL + t));
                         }
-                        issue_s(t, (j + 1) % C::STAGES);
-                        mma_commit(bar(C::B_SFULL + t));
-                    } else {
-                        mma_commit(bar(C::B_OFULL + t));
+                }
+                for (int j = 0; ok && j < n_iter; ++j) {
+                    const int s = j % C::STAGES;
+                    if (!(ok = wait_bar(wc, bar(C::B_VFULL + s), (j / C::STAGES) & 1))) break;
+                    bool next_k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= nkv[t]) continue;
+                        if (!(ok = wait_bar(wc, bar(C::B_PFULL + t), j & 1))) break;
+                        tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        if (j + 1 < nkv[t]) {
+                            if (!next_k_ready) {
+                                const int s1 = (j + 1) % C::STAGES;
+                                if (!(ok = wait_bar(wc, bar(C::B_KFULL + s1), ((j + 1) / C::STAGES) & 1)))
+                                    break;
+                                tc_fence_after();
+                                next_k_ready = true;
+                            }
+                            issue_s(t, (j + 1) % C::STAGES);
+                            mma_commit(bar(C::B_SFULL + t));
+                        } else {
+                            mma_commit(bar(C::B_OFULL + t));
+                        }
+                    }
+                    mma_commit(bar(C::B_KVEMPTY + s));
+                }
+                // make sure no MMA is still reading smem / writing TMEM at teardown
+                mma_commit(bar(C::B_DRAIN));
+                drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+            }
+        }
+    } else {
+        if (!skip) {
+            // ------------------------------------------------------------ softmax warpgroups
+            const int t = (warp - 4) >> 2;
+            const int wq = warp & 3;                 // TMEM lane quarter of this warp
+            const int r = wq * 32 + lane;            // row within the tile
+            const int row = q0 + kTile * t + r;      // row within the head
+            const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+            const uint32_t s_addr = tmem + lane_off + C::s_col(t);
+            const uint32_t o_addr = tmem + lane_off + C::o_col(t);
+            const float cs = args.scale_log2;
+            float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
+            float l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nkv[t]; ++j) {
+                ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[128];
+                tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+                tmem_ld_wait();
+                float* sv = reinterpret_cast<float*>(sr);
+                // mask: key tail (keys >= N) and, on the diagonal block, keys > row
+                int limit = N - j * kTile;
+                if (CAUSAL) limit = min(limit, row - j * kTile + 1);
+                if (limit < kTile) {
+    #pragma unroll
+                    for (int c = 0; c < kTile; ++c)
+                        if (c >= limit) sv[c] = -INFINITY;
+                }
+                // row max: four independent chains of 3-input max
+                float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+    #pragma unroll
+                for (int c = 4; c < kTile; c += 8) {
+                    mx0 = max3(mx0, sv[c], sv[c + 1]);
+                    mx1 = max3(mx1, sv[c + 2], sv[c + 3]);
+                    mx2 = max3(mx2, sv[c + 4], sv[c + 5]);
+                    mx3 = max3(mx3, sv[c + 6], sv[c + 7]);
+                }
+                mx0 = max3(mx0, sv[124], sv[125]);
+                mx1 = max3(mx1, sv[126], sv[127]);
+                const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs);
+                const bool move = m_new > m_ref + 8.0f;
+                float alpha = 1.0f;
+                if (move) {
+                    alpha = ex2_approx(m_ref - m_new);  // 0 on the first block
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                // p = exp2(s tau log2e - m_ref), two columns per FMA / add instruction
+                const uint64_t cs2 = f2_pack(cs, cs);
+                const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+                uint64_t sum2 = f2_pack(0.f, 0.f);
+    #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+    #pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const uint64_t arg = f2_fma(f2_pack(sv[64 * h + 2 * e], sv[64 * h + 2 * e + 1]), cs2, nm2);
+                        float a0, a1;
+                        f2_unpack(arg, a0, a1);
+                        const float p0 = ex2_approx(a0);
+                        const float p1 = ex2_approx(a1);
+                        sum2 = f2_add(sum2, f2_pack(p0, p1));
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st32(s_addr + 32 * h, pk);
+                }
+                float sum0, sum1;
+                f2_unpack(sum2, sum0, sum1);
+                l += sum0 + sum1;
+                // Rescale O after the P stores, when the S registers are dead.  O holds
+                // P V up to block j-1 (S of block j was committed after that MMA).
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+    #pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_addr + c, orr);
+                        tmem_ld_wait();
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(o_addr + c, orr);
                     }
                 }
-                mma_commit(bar(C::B_KVEMPTY + s));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL + t));
             }
-            // make sure no MMA is still reading smem / writing TMEM at teardown
-            mma_commit(bar(C::B_DRAIN));
-            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
-        }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int t = (warp - 4) >> 2;
-        const int wq = warp & 3;                 // TMEM lane quarter of this warp
-        const int r = wq * 32 + lane;            // row within the tile
-        const int row = q0 + kTile * t + r;      // row within the head
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t s_addr = tmem + lane_off + C::s_col(t);
-        const uint32_t o_addr = tmem + lane_off + C::o_col(t);
-        const float cs = args.scale_log2;
-        float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
-        float l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nkv[t]; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-            tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-            tmem_ld_wait();
-            float* sv = reinterpret_cast<float*>(sr);
-            // mask: key tail (keys >= N) and, on the diagonal block, keys > row
-            int limit = N - j * kTile;
-            if (CAUSAL) limit = min(limit, row - j * kTile + 1);
-            if (limit < kTile) {
-#pragma unroll
-                for (int c = 0; c < kTile; ++c)
-                    if (c >= limit) sv[c] = -INFINITY;
-            }
-            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
-#pragma unroll
-            for (int c = 4; c < kTile; c += 4) {
-                mx0 = fmaxf(mx0, sv[c]);
-                mx1 = fmaxf(mx1, sv[c + 1]);
-                mx2 = fmaxf(mx2, sv[c + 2]);
-                mx3 = fmaxf(mx3, sv[c + 3]);
-            }
-            const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs);
-            const bool move = m_new > m_ref + 8.0f;
-            float alpha = 1.0f;
-            if (move) {
-                alpha = ex2_approx(m_ref - m_new);  // 0 on the first block
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float nm = -m_ref;
-            float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(sv[64 * h + 2 * e], cs, nm));
-                    const float p1 = ex2_approx(fmaf(sv[64 * h + 2 * e + 1], cs, nm));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[e] = pack2<BF16>(p0, p1);
-                }
-                tmem_st32(s_addr + 32 * h, pk);
-            }
-            l += sum0 + sum1;
-            // Rescale O after the P stores, when the S registers are dead.  O holds
-            // P V up to block j-1 (S of block j was committed after that MMA).
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-#pragma unroll
+            // ------------------------------------------------------------ epilogue
+            if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
+            if (ok && nkv[t] > 0) {
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                const bool valid = row < N;
+                using Vec = uint4;
+                Vec* dst = reinterpret_cast<Vec*>(static_cast<uint16_t*>(args.o) +
+                                                  (static_cast<size_t>(bh) * N + row) * D);
+    #pragma unroll
                 for (int c = 0; c < D; c += 32) {
                     uint32_t orr[32];
                     tmem_ld32(o_addr + c, orr);
                     tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(o_addr + c, orr);
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                            __uint_as_float(orr[2 * e + 1]) * inv_l);
+                    if (valid) {
+    #pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[c / 8 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                         pk[4 * v4 + 3]);
+                    }
                 }
+                if (valid)
+                    args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL + t));
-        }
-        // ------------------------------------------------------------ epilogue
-        if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
-        if (ok && nkv[t] > 0) {
-            tc_fence_after();
-            const float inv_l = 1.0f / l;
-            const bool valid = row < N;
-            using Vec = uint4;
-            Vec* dst = reinterpret_cast<Vec*>(static_cast<uint16_t*>(args.o) +
-                                              (static_cast<size_t>(bh) * N + row) * D);
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t orr[32];
-                tmem_ld32(o_addr + c, orr);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
-                                        __uint_as_float(orr[2 * e + 1]) * inv_l);
-                if (valid) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[c / 8 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                     pk[4 * v4 + 3]);
-                }
-            }
-            if (valid)
-                args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
         }
     }
 
@@ -360,7 +373,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const dim3 grid = head_major_grid(a.num_qblocks, BH);
+    const dim3 grid = lpt_grid(a.num_qblocks, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }

@@ -193,8 +193,18 @@ def test_timeout_path_reports_and_context_survives():
     _compare_head(x, out, 0, 0, False, 0.125, backward=False)
 
 
-def test_repeated_calls_deterministic_forward():
-    x = make_inputs(1, 4, 1024, 128, seed=21, with_grad=False)
-    a = _run_gpu(x, True, 128 ** -0.5, backward=False)
-    b = _run_gpu(x, True, 128 ** -0.5, backward=False)
-    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+def test_repeated_calls_are_stable():
+    """Every launch gives the same bits for O, lse, dK and dV (none of them is
+    summed across CTAs) and finite dQ: catches intermittent launch-wide
+    failures, which a single parity run can miss."""
+    w = WORKLOADS["fwdbwd_causal_b1_h8_n32768_d128"]
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed)
+    first = None
+    for _ in range(6):
+        out = _run_gpu(x, True, w.scale, backward=True)
+        assert torch.isfinite(out["dq"].float()).all()
+        if first is None:
+            first = out
+            assert torch.isfinite(out["o"].float()).all() and torch.isfinite(out["lse"]).all()
+        for name in ("o", "lse", "dk", "dv"):
+            assert torch.equal(out[name], first[name]), name
