@@ -1,7 +1,8 @@
 """Benchmark: exact attention forward + backward on GB300.
 
-One step = one pass of the whole hot path over one batch: attn_fwd,
-attn_bwd_preprocess and attn_bwd (main kernel + dQ convert) on the causal
+One step = one pass of the whole hot path over one batch: attn_fwd_train
+(O in bf16 and fp32, lse), attn_bwd_preprocess_o32 (D = rowsum(dO o O)) and
+attn_bwd (main kernel + dQ convert) on the causal
 B=2 H=16 N=8192 d=128 workload (Q, K scaled by 3 for peaked softmax rows),
 bf16 inputs resident in HBM.  FLOPs per step follow the stated convention:
 forward 4*B*H*N^2*d, forward+backward 10*B*H*N^2*d, each halved for causal.
@@ -139,6 +140,7 @@ def run_ours(args):
     x = make_inputs(B, H, N, d, w.seed + 100 * rank, w.qk_mult)
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
     o = torch.empty_like(q)
+    o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     D = torch.empty_like(lse)
     acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
@@ -152,11 +154,10 @@ def run_ours(args):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+        attn.attn_fwd_train(P(q), P(k), P(v), P(o), P(o32), P(lse), B, H, N, d, causal, scale, s)
         if ev:
             ev[1].record(stream)
-        attn.attn_bwd_preprocess(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), B, H, N, d,
-                                 causal, scale, s)
+        attn.attn_bwd_preprocess_o32(P(o32), P(dO), P(D), P(acc), B, H, N, d, s)
         if ev:
             ev[2].record(stream)
         attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
@@ -191,6 +192,22 @@ def run_ours(args):
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
     ms_step = dist_max(sum(t_step) / len(t_step), dev)
 
+    # forward alone (attn_fwd: O and lse, no fp32 O), the inference forward,
+    # timed per launch with the same L2 flush between launches
+    for _ in range(3):
+        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        fevs[i][0].record(stream)
+        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+        fevs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during the forward-only launches")
+    ms_fwd_only = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in fevs), dev)
+
     # end to end through the public API: pinned host inputs in, results out
     e2e = None
     if args.e2e_steps > 0:
@@ -202,9 +219,10 @@ def run_ours(args):
         def e2e_step():
             for kk in dx:
                 dx[kk].copy_(hx[kk], non_blocking=True)
-            oo, ll = attn.forward(dx["q"], dx["k"], dx["v"], causal, scale, o=o, lse=lse)
+            oo, ll, o32_ = attn.forward(dx["q"], dx["k"], dx["v"], causal, scale, o=o, lse=lse,
+                                        o32=o32)
             attn.backward(dx["q"], dx["k"], dx["v"], oo, ll, dx["dO"], causal, scale,
-                          dq=dq, dk=dk, dv=dv, D=D, dq_accum=acc)
+                          dq=dq, dk=dk, dv=dv, D=D, dq_accum=acc, o32=o32_)
             for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
                 hout[n].copy_(t, non_blocking=True)
         for _ in range(2):
@@ -228,7 +246,8 @@ def run_ours(args):
     tflops_fb = whole_job_rate(world, flops_fb, ms_step) / 1e12
     ms_fwd = statistics.mean(t_fwd)
     ms_bwd = statistics.mean(t_bwd)
-    tflops_fwd = w.flops_fwd() / (ms_fwd * 1e-3) / 1e12
+    tflops_fwd = whole_job_rate(world, w.flops_fwd(), ms_fwd_only) / 1e12
+    tflops_fwd_train = w.flops_fwd() / (ms_fwd * 1e-3) / 1e12
     # dominant kernel: the backward main kernel (timed with its dQ convert);
     # algorithmic work = 5 MMAs x 2 N^2 d per head, halved for causal
     flops_bwd_kernel = 10.0 * B * H * N * N * d / (2 if causal else 1)
@@ -256,8 +275,11 @@ def run_ours(args):
                    "l2": "inputs 268 MB > 126 MB L2, and L2 flushed (512 MB write) between steps",
                    "flop_convention": "fwd 4BHN^2d, fwd+bwd 10BHN^2d, halved for causal"},
         "frac_of_peak": round(tflops_fb / peak_sus, 4),
-        "fwd": {"tflops": round(tflops_fwd, 2), "ms": round(ms_fwd, 4),
-                "frac_of_peak": round(tflops_fwd / peak_burst, 4), "peak": peak_burst},
+        "fwd": {"kernel": "attn_fwd (O, lse)", "tflops": round(tflops_fwd, 2),
+                "ms": round(ms_fwd_only, 4), "frac_of_peak": round(tflops_fwd / peak_burst, 4),
+                "peak": peak_burst, "peak_kind": "bf16 burst, %s" % peaks["source"]},
+        "fwd_train": {"kernel": "attn_fwd_train (O, fp32 O, lse), inside the step",
+                      "tflops": round(tflops_fwd_train, 2), "ms": round(ms_fwd, 4)},
         "fwd_bwd_14x_tflops": round(world * 14.0 * B * H * N * N * d / 2 / (ms_step * 1e-3) / 1e12, 2),
         "bwd_preprocess_ms": round(statistics.mean(t_pre), 4),
         "roofline": {"kernel": "attn_bwd (main kernel + dQ convert)", "bound": "tensor",

@@ -69,6 +69,21 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * Forward pass for training: as attn_fwd, and additionally writes o32
+ * [B,H,N,d] fp32, the same O before its rounding to 16 bits, for
+ * attn_bwd_preprocess_o32 (the backward saves O, sj-techlog page, backward
+ * section; here at accumulation precision).  In both forward entry points
+ * each output row is normalised by the sum of the probabilities as rounded
+ * for the P V product, so its weights sum to exactly 1; lse uses the exact
+ * fp32 sum.  o32 must be non-NULL and 16-byte aligned.
+ */
+int attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
+                   int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_train_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                       float* lse, int B, int H, int N, int d, int causal, float scale,
+                       void* stream);
+
+/*
  * Backward pre-processing.  Computes the softmax-gradient row term
  *   D_i = sum_j P_ij dP_ij,   P_ij = exp(s_ij - lse_i),   dP = dO V^T
  * (wonbeomjang.kr FlashAttention-2 review, "Backward Pass": D_i is the sum
@@ -91,6 +106,20 @@ int attn_bwd_preprocess(const void* q, const void* k, const void* v, const void*
 int attn_bwd_preprocess_f16(const void* q, const void* k, const void* v, const void* dO,
                             const float* lse, float* D, float* dq_accum,
                             int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Backward pre-processing from the forward's fp32 O (the FlashAttention-2
+ * review's D_i = rowsum(dO_i o O_i), "Backward Pass" of FlashAttention-2):
+ * reads o32 [B,H,N,d] fp32 (from attn_fwd_train) and dO [B,H,N,d] 16-bit,
+ * writes D [B,H,N] and zeroes dq_accum.  A memory-bound pass; gives the same
+ * D as attn_bwd_preprocess to within the output tolerance, including on
+ * nearly one-hot rows, because o32's weights sum to exactly 1.  Must precede
+ * attn_bwd on the same stream.
+ */
+int attn_bwd_preprocess_o32(const float* o32, const void* dO, float* D, float* dq_accum,
+                            int B, int H, int N, int d, void* stream);
+int attn_bwd_preprocess_o32_f16(const float* o32, const void* dO, float* D, float* dq_accum,
+                                int B, int H, int N, int d, void* stream);
 
 /*
  * Backward pass (recomputation of S and P from lse, sj-techlog page, section

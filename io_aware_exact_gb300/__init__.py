@@ -53,8 +53,13 @@ def lib():
             fwd = [P, P, P, P, P, I, I, I, I, I, F, P]
             pre = [P, P, P, P, P, P, P, I, I, I, I, I, F, P]
             bwd = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+            fwdt = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+            pre32 = [P, P, P, P, I, I, I, I, P]
             for name, at in (("attn_fwd", fwd), ("attn_fwd_f16", fwd),
+                             ("attn_fwd_train", fwdt), ("attn_fwd_train_f16", fwdt),
                              ("attn_bwd_preprocess", pre), ("attn_bwd_preprocess_f16", pre),
+                             ("attn_bwd_preprocess_o32", pre32),
+                             ("attn_bwd_preprocess_o32_f16", pre32),
                              ("attn_bwd", bwd), ("attn_bwd_f16", bwd)):
                 fn = getattr(L, name)
                 fn.argtypes = at
@@ -98,6 +103,17 @@ def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream, f16=False):
     fn = lib().attn_fwd_f16 if f16 else lib().attn_fwd
     _check(fn(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale), stream),
            "attn_fwd")
+
+
+def attn_fwd_train(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, f16=False):
+    fn = lib().attn_fwd_train_f16 if f16 else lib().attn_fwd_train
+    _check(fn(q, k, v, o, o32, lse, B, H, N, d, int(bool(causal)), float(scale), stream),
+           "attn_fwd_train")
+
+
+def attn_bwd_preprocess_o32(o32, dO, D, dq_accum, B, H, N, d, stream, f16=False):
+    fn = lib().attn_bwd_preprocess_o32_f16 if f16 else lib().attn_bwd_preprocess_o32
+    _check(fn(o32, dO, D, dq_accum, B, H, N, d, stream), "attn_bwd_preprocess_o32")
 
 
 def attn_bwd_preprocess(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream,
@@ -152,24 +168,36 @@ def _check_qkv(*ts):
     return t0.shape, t0.dtype == torch.float16
 
 
-def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=None):
-    """O, lse for [B,H,N,d] CUDA tensors (outputs allocated by torch if not given)."""
+def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=None,
+            o32=None):
+    """O, lse for [B,H,N,d] CUDA tensors (outputs allocated by torch if not given).
+
+    With ``o32`` (an fp32 [B,H,N,d] tensor, or True to allocate one) the
+    training forward also writes O in fp32 and returns (o, lse, o32).
+    """
     torch = _torch()
     (B, H, N, d), f16 = _check_qkv(q, k, v)
     scale = d ** -0.5 if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-             B, H, N, d, causal, scale, _stream_handle(stream), f16)
-    return o, lse
+    if o32 is None:
+        attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                 B, H, N, d, causal, scale, _stream_handle(stream), f16)
+        return o, lse
+    if o32 is True:
+        o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    attn_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o32.data_ptr(),
+                   lse.data_ptr(), B, H, N, d, causal, scale, _stream_handle(stream), f16)
+    return o, lse, o32
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=None, dv=None,
-             D=None, dq_accum=None, stream=None):
+             D=None, dq_accum=None, stream=None, o32=None):
     """dQ, dK, dV for [B,H,N,d] CUDA tensors (workspace allocated by torch if not given).
 
-    ``o`` (the forward output) is not read and may be None: the preprocess
-    recomputes D from q, k, v, dO and lse.
+    With ``o32`` (the fp32 O of the training forward) D comes from
+    rowsum(dO o O); otherwise the preprocess recomputes it from q, k, v, dO
+    and lse.  ``o`` (the 16-bit forward output) is not read and may be None.
     """
     torch = _torch()
     (B, H, N, d), f16 = _check_qkv(q, k, v, dO)
@@ -181,8 +209,13 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
     if dq_accum is None:
         dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
     s = _stream_handle(stream)
-    attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
-                        D.data_ptr(), dq_accum.data_ptr(), B, H, N, d, causal, scale, s, f16)
+    if o32 is not None:
+        attn_bwd_preprocess_o32(o32.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(),
+                                B, H, N, d, s, f16)
+    else:
+        attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(),
+                            lse.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), B, H, N, d,
+                            causal, scale, s, f16)
     attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
              B, H, N, d, causal, scale, s, f16)
@@ -195,7 +228,7 @@ def _autograd_function():
     class AttnFunction(torch.autograd.Function):
         """Exact attention with the library's forward and backward kernels.
 
-        Saves q, k, v and lse (O(N) extra per row, no N x N buffer) and
+        Saves q, k, v, lse and the fp32 O (O(N d) extra, no N x N buffer) and
         recomputes P in the backward, like the FlashAttention autograd
         function described on the sj-techlog page ("1. Python interface는
         scale·RNG state·작은 통계를 autograd에 넘긴다").
@@ -204,15 +237,16 @@ def _autograd_function():
         @staticmethod
         def forward(ctx, q, k, v, causal=False, scale=None):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-            o, lse = forward(q, k, v, causal, scale)
-            ctx.save_for_backward(q, k, v, lse)
+            o, lse, o32 = forward(q, k, v, causal, scale, o32=True)
+            ctx.save_for_backward(q, k, v, lse, o32)
             ctx.causal, ctx.scale = causal, scale
             return o
 
         @staticmethod
         def backward(ctx, dO):
-            q, k, v, lse = ctx.saved_tensors
-            dq, dk, dv = backward(q, k, v, None, lse, dO.contiguous(), ctx.causal, ctx.scale)
+            q, k, v, lse, o32 = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, None, lse, dO.contiguous(), ctx.causal, ctx.scale,
+                                  o32=o32)
             return dq, dk, dv, None, None
 
     return AttnFunction

@@ -123,9 +123,10 @@ int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
 
 int map_launch(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int d, int causal, float scale, void* stream, bool bf16) {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse, int B,
+             int H, int N, int d, int causal, float scale, void* stream, bool bf16) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (o32 != nullptr && !aligned16(o32)) return ATTN_ERR_MISALIGNED;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
     if ((rc = check_scale(scale))) return rc;
@@ -140,6 +141,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
         return rc;
     FwdArgs a{};
     a.o = o;
+    a.o32 = o32;
     a.lse = lse;
     a.status = status;
     a.N = N;
@@ -179,6 +181,25 @@ int pre_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.timeout_ns = kDefaultTimeoutNs;
     return map_launch(launch_bwd_preprocess(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+int pre_o32_impl(const float* o32, const void* dO, float* D, float* dq_accum, int B, int H, int N,
+                 int d, void* stream, bool bf16) {
+    if (!o32 || !dO || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
+    int rc = check_shape(B, H, N, d);
+    if (rc) return rc;
+    if (!aligned16(o32) || !aligned16(dO) || !aligned16(D) || !aligned16(dq_accum))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    PreO32Args a{};
+    a.o32 = o32;
+    a.dO = dO;
+    a.D = D;
+    a.dq_accum = dq_accum;
+    a.rows = static_cast<long long>(B) * H * N;
+    a.d = d;
+    return map_launch(launch_bwd_preprocess_o32(a, bf16, static_cast<cudaStream_t>(stream)));
 }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
@@ -250,12 +271,35 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, int causal, float scale, void* stream) {
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, stream, true);
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, N, d, causal, scale, stream, true);
 }
 
 int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, int causal, float scale, void* stream) {
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, stream, false);
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, N, d, causal, scale, stream, false);
+}
+
+int attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
+                   int B, int H, int N, int d, int causal, float scale, void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, true);
+}
+
+int attn_fwd_train_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                       float* lse, int B, int H, int N, int d, int causal, float scale,
+                       void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, false);
+}
+
+int attn_bwd_preprocess_o32(const float* o32, const void* dO, float* D, float* dq_accum, int B,
+                            int H, int N, int d, void* stream) {
+    return pre_o32_impl(o32, dO, D, dq_accum, B, H, N, d, stream, true);
+}
+
+int attn_bwd_preprocess_o32_f16(const float* o32, const void* dO, float* D, float* dq_accum,
+                                int B, int H, int N, int d, void* stream) {
+    return pre_o32_impl(o32, dO, D, dq_accum, B, H, N, d, stream, false);
 }
 
 int attn_bwd_preprocess(const void* q, const void* k, const void* v, const void* dO,

@@ -305,6 +305,47 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // ============================================================================
+// 1c. preprocess from the forward's fp32 O: D_i = sum_k dO_ik O_ik, dq_accum := 0
+// ============================================================================
+// The FlashAttention-2 review's form of D ("Backward Pass" of FlashAttention-2:
+// D_i = rowsum(dO_i o O_i)), evaluated with the fp32 copy of O that
+// attn_fwd_train writes.  That O is normalised by the sum of the rounded P
+// that multiplied V, so its weights sum to exactly 1 and D matches the P the
+// backward recomputes even on nearly one-hot rows.  Memory-bound: one pass
+// over O (fp32) and dO, plus zeroing dq_accum.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_o32_kernel(const PreO32Args a) {
+    constexpr int TPR = D / 8;  // threads per row, 8 elements each
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const int sub = threadIdx.x % TPR;
+    const long long rows_per_sweep = nthreads / TPR;
+    const long long sweeps = (a.rows + rows_per_sweep - 1) / rows_per_sweep;
+    // every thread runs the same number of sweeps, so the row-group shuffles
+    // below always see all 32 lanes of the warp
+    for (long long sw = 0; sw < sweeps; ++sw) {
+        const long long row = sw * rows_per_sweep + tid / TPR;
+        const bool valid = row < a.rows;
+        float acc = 0.f;
+        if (valid) {
+            const float4* o4 = reinterpret_cast<const float4*>(a.o32 + row * D + sub * 8);
+            const float4 x0 = o4[0], x1 = o4[1];
+            const uint4 d4 = reinterpret_cast<const uint4*>(a.dO)[row * TPR + sub];
+            const uint16_t* dh = reinterpret_cast<const uint16_t*>(&d4);
+            const float ov[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(ov[e], to_f32<BF16>(dh[e]), acc);
+            float4* z = reinterpret_cast<float4*>(a.dq_accum + row * D + sub * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+        if (valid && sub == 0) a.D[row] = acc;
+    }
+}
+
+// ============================================================================
 // 2. main backward kernel
 // ============================================================================
 // One CTA = one (b, h) and one 128-key block j; it loops over the 128-query
@@ -762,6 +803,24 @@ static int sm_count() {
         if (n <= 0) n = 152;
     }
     return n;
+}
+
+cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream) {
+    const long long rows_per_block = 256 / (a.d / 8);
+    long long blocks = (a.rows + rows_per_block - 1) / rows_per_block;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (a.d == 64) {
+        if (bf16) attn_bwd_preprocess_o32_kernel<true, 64><<<blocks, 256, 0, stream>>>(a);
+        else attn_bwd_preprocess_o32_kernel<false, 64><<<blocks, 256, 0, stream>>>(a);
+    } else if (a.d == 128) {
+        if (bf16) attn_bwd_preprocess_o32_kernel<true, 128><<<blocks, 256, 0, stream>>>(a);
+        else attn_bwd_preprocess_o32_kernel<false, 128><<<blocks, 256, 0, stream>>>(a);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream) {

@@ -21,6 +21,7 @@ constexpr int kBoxBytes = kTile * kBoxCols * 2;  // 16 KB
 
 struct FwdArgs {
     void* o;               // [B*H, N, d] 16-bit, written
+    float* o32;            // [B*H, N, d] fp32 copy of O for the backward, or nullptr
     float* lse;            // [B*H, N] fp32, written (natural log, scale inside)
     int* status;           // device status word
     int N;                 // sequence length
@@ -56,6 +57,15 @@ struct DsumArgs {
     unsigned long long timeout_ns;
 };
 
+struct PreO32Args {
+    const float* o32;      // [B*H, N, d] fp32 O from attn_fwd_train
+    const void* dO;        // [B*H, N, d] 16-bit
+    float* D;              // [B*H, N]
+    float* dq_accum;       // [B*H, N, d] fp32, zeroed
+    long long rows;        // B*H*N
+    int d;
+};
+
 struct DqConvertArgs {
     const float* dq_accum;  // [B*H, N, d]
     void* dq;               // [B*H, N, d] 16-bit
@@ -73,6 +83,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const DsumArgs& a, int BH, int d, bool causal,
                             bool bf16, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
 
 // Grid layout shared by the attention kernels: x = (batch, head), y/z = block

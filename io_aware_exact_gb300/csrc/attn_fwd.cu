@@ -63,7 +63,7 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
@@ -244,7 +244,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t o_addr = tmem + lane_off + C::o_col(t);
             const float cs = args.scale_log2;
             float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
-            float l = 0.f;
+            float l = 0.f;            // sum of p (fp32): the normaliser inside lse
+            float lb = 0.f;           // sum of p as rounded for the PV MMA: normalises O
             bool ok = true;
             for (int j = 0; j < nkv[t]; ++j) {
                 ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
@@ -282,30 +283,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (move) {
                     alpha = ex2_approx(m_ref - m_new);  // 0 on the first block
                     l *= alpha;
+                    lb *= alpha;
                     m_ref = m_new;
                 }
                 // p = exp2(s tau log2e - m_ref), two columns per FMA / add instruction
                 const uint64_t cs2 = f2_pack(cs, cs);
                 const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t sum2 = f2_pack(0.f, 0.f);
+                uint64_t sumb2 = f2_pack(0.f, 0.f);
+                // TRAIN also sums the rounded p (one more unpack and add per pair);
+                // it stores P in 16-column pieces (32 values) to keep that in registers.
+                constexpr int PW = TRAIN ? 32 : 64;  // p values per TMEM store
     #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
+                for (int h = 0; h < 128 / PW; ++h) {
+                    uint32_t pk[PW / 2];
     #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const uint64_t arg = f2_fma(f2_pack(sv[64 * h + 2 * e], sv[64 * h + 2 * e + 1]), cs2, nm2);
+                    for (int e = 0; e < PW / 2; ++e) {
+                        const uint64_t arg = f2_fma(f2_pack(sv[PW * h + 2 * e], sv[PW * h + 2 * e + 1]), cs2, nm2);
                         float a0, a1;
                         f2_unpack(arg, a0, a1);
                         const float p0 = ex2_approx(a0);
                         const float p1 = ex2_approx(a1);
                         sum2 = f2_add(sum2, f2_pack(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
+                        if constexpr (TRAIN) sumb2 = f2_add(sumb2, unpack2_f2<BF16>(pk[e]));
                     }
-                    tmem_st32(s_addr + 32 * h, pk);
+                    if constexpr (TRAIN)
+                        tmem_st16(s_addr + PW / 2 * h, pk);
+                    else
+                        tmem_st32(s_addr + PW / 2 * h, pk);
                 }
                 float sum0, sum1;
                 f2_unpack(sum2, sum0, sum1);
                 l += sum0 + sum1;
+                if constexpr (TRAIN) {
+                    f2_unpack(sumb2, sum0, sum1);
+                    lb += sum0 + sum1;
+                }
                 // Rescale O after the P stores, when the S registers are dead.  O holds
                 // P V up to block j-1 (S of block j was committed after that MMA).
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -328,26 +342,39 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
             if (ok && nkv[t] > 0) {
                 tc_fence_after();
-                const float inv_l = 1.0f / l;
+                // TRAIN normalises O by the sum of the rounded p that actually
+                // multiplied V, so each fp32 output row is a convex combination of V
+                // rows (weights summing to 1) and rowsum(dO o O) matches the P the
+                // backward recomputes; lse keeps the exact sum either way.
+                const float inv_l = 1.0f / (TRAIN ? lb : l);
                 const bool valid = row < N;
                 using Vec = uint4;
                 Vec* dst = reinterpret_cast<Vec*>(static_cast<uint16_t*>(args.o) +
                                                   (static_cast<size_t>(bh) * N + row) * D);
+                float4* dst32 = !TRAIN ? nullptr
+                                : reinterpret_cast<float4*>(args.o32 + (static_cast<size_t>(bh) * N + row) * D);
     #pragma unroll
                 for (int c = 0; c < D; c += 32) {
                     uint32_t orr[32];
                     tmem_ld32(o_addr + c, orr);
                     tmem_ld_wait();
+    #pragma unroll
+                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * inv_l);
                     uint32_t pk[16];
     #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
-                                            __uint_as_float(orr[2 * e + 1]) * inv_l);
+                        pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1]));
                     if (valid) {
     #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4)
                             dst[c / 8 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
                                                          pk[4 * v4 + 3]);
+                        if constexpr (TRAIN) {
+    #pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4)
+                                dst32[c / 4 + v4] = make_float4(__uint_as_float(orr[4 * v4]), __uint_as_float(orr[4 * v4 + 1]),
+                                                                __uint_as_float(orr[4 * v4 + 2]), __uint_as_float(orr[4 * v4 + 3]));
+                        }
                     }
                 }
                 if (valid)
@@ -364,12 +391,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const FwdArgs& a, int BH,
                                 cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = attn_fwd_kernel<D, CAUSAL, BF16>;
+    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -382,7 +409,9 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const FwdArgs& a, int BH, int d, bool causal, bool bf16,
                        cudaStream_t stream) {
 #define ATTN_FWD_CASE(D_, C_, B_) \
-    if (d == D_ && causal == C_ && bf16 == B_) return launch_fwd_t<D_, C_, B_>(tq, tk, tv, a, BH, stream);
+    if (d == D_ && causal == C_ && bf16 == B_)                                  \
+        return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true>(tq, tk, tv, a, BH, stream) \
+                                : launch_fwd_t<D_, C_, B_, false>(tq, tk, tv, a, BH, stream);
     ATTN_FWD_CASE(64, false, true)
     ATTN_FWD_CASE(64, true, true)
     ATTN_FWD_CASE(128, false, true)

@@ -379,6 +379,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// The two 16-bit floats of a packed pair, as fp32 (lo = bits 0..15).
+template <bool kBF16>
+__device__ __forceinline__ uint64_t unpack2_f2(uint32_t v) {
+    if constexpr (kBF16) {
+        return f2_pack(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+    } else {
+        float lo, hi;
+        asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+            : "=f"(lo), "=f"(hi) : "r"(v));
+        return f2_pack(lo, hi);
+    }
+}
+
 template <bool kBF16>
 __device__ __forceinline__ float to_f32(uint16_t h) {
     if constexpr (kBF16) {

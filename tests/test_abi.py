@@ -80,6 +80,18 @@ def test_forward_argument_errors(L):
     assert L.attn_fwd_f16(None, A, A, A, A, 1, 1, 1, 64, 0, 1.0, None) == 1
 
 
+def test_training_entry_point_argument_errors(L):
+    args = (A, A, A, A, A, A, 1, 1, 128, 64, 0, 0.125, None)
+    assert L.attn_fwd_train(*args) in (4, 0)  # valid arguments: no device here
+    bad = list(args); bad[4] = None
+    assert L.attn_fwd_train(*bad) == 1          # o32 is required
+    bad = list(args); bad[4] = A + 4
+    assert L.attn_fwd_train(*bad) == 3
+    assert L.attn_bwd_preprocess_o32(None, A, A, A, 1, 1, 128, 64, None) == 1
+    assert L.attn_bwd_preprocess_o32(A, A, A, A, 1, 1, 128, 80, None) == 2
+    assert L.attn_bwd_preprocess_o32(A + 8, A, A, A, 1, 1, 128, 64, None) == 3
+
+
 def test_backward_argument_errors(L):
     assert _bwd(L, dq=None) == 1
     assert _bwd(L, acc=None) == 1

@@ -23,14 +23,24 @@ def _f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def _run_gpu(x, causal, scale, backward, f16=False):
+def _run_gpu(x, causal, scale, backward, f16=False, path="train"):
+    """path "train": attn_fwd_train + attn_bwd_preprocess_o32 + attn_bwd (the
+    training path bench.py times); path "exact": attn_fwd +
+    attn_bwd_preprocess (D from recomputed P and dP) + attn_bwd."""
     dev = torch.device("cuda:0")
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    o, lse = attn.forward(q, k, v, causal, scale)
+    if path == "train":
+        o, lse, o32 = attn.forward(q, k, v, causal, scale, o32=True)
+    else:
+        o, lse = attn.forward(q, k, v, causal, scale)
+        o32 = None
     out = {"o": o, "lse": lse}
+    if o32 is not None:
+        # the 16-bit O is the rounding of the fp32 O
+        assert torch.equal(o32.to(o.dtype), o)
     if backward:
         dO = x["dO"].to(dev)
-        dq, dk, dv = attn.backward(q, k, v, o, lse, dO, causal, scale)
+        dq, dk, dv = attn.backward(q, k, v, o, lse, dO, causal, scale, o32=o32)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert attn.attn_get_device_status() == 0
@@ -90,10 +100,11 @@ def test_forward_small(B, H, N, d, causal):
             _compare_head(x, out, b, h, causal, d ** -0.5, backward=False)
 
 
+@pytest.mark.parametrize("path", ["train", "exact"])
 @pytest.mark.parametrize("B,H,N,d,causal", SMALL)
-def test_backward_small(B, H, N, d, causal):
+def test_backward_small(B, H, N, d, causal, path):
     x = make_inputs(B, H, N, d, seed=11 + N + d)
-    out = _run_gpu(x, causal, d ** -0.5, backward=True)
+    out = _run_gpu(x, causal, d ** -0.5, backward=True, path=path)
     for b in range(B):
         for h in range(H):
             _compare_head(x, out, b, h, causal, d ** -0.5, backward=True)
@@ -115,10 +126,12 @@ def test_fp16_entry_points():
         _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
 
 
-def test_peaked_rows_forward():
-    """Q, K scaled by 8: softmax rows close to one-hot stress the max/rescale."""
+@pytest.mark.parametrize("path", ["train", "exact"])
+def test_peaked_rows(path):
+    """Q, K scaled by 8: softmax rows close to one-hot stress the max/rescale
+    and the cancellation in dS = P (dP - D)."""
     x = make_inputs(1, 2, 1024, 128, seed=13, qk_mult=8.0)
-    out = _run_gpu(x, True, 128 ** -0.5, backward=True)
+    out = _run_gpu(x, True, 128 ** -0.5, backward=True, path=path)
     for h in range(2):
         _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
 
@@ -148,6 +161,34 @@ def test_workload(name, nheads):
     out = _run_gpu(x, w.causal, w.scale, backward=w.backward)
     for (b, h) in _heads(w, nheads, w.seed):
         _compare_head(x, out, b, h, w.causal, w.scale, w.backward)
+
+
+def test_workload_peaked_exact_preprocess():
+    """The headline workload through the exact-D preprocess (no fp32 O)."""
+    w = WORKLOADS["fwdbwd_causal_peaked_b2_h16_n8192_d128"]
+    x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    out = _run_gpu(x, w.causal, w.scale, backward=True, path="exact")
+    for (b, h) in _heads(w, 2, w.seed + 1):
+        _compare_head(x, out, b, h, w.causal, w.scale, True)
+
+
+def test_autograd_function():
+    """attention() as a torch.autograd.Function: gradients through .backward()."""
+    x = make_inputs(1, 2, 300, 64, seed=17)
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev).requires_grad_(True) for n in ("q", "k", "v"))
+    o = attn.attention(q, k, v, True)
+    o.backward(x["dO"].to(dev))
+    out = {"o": o.detach().cpu(), "dq": q.grad.cpu(), "dk": k.grad.cpu(), "dv": v.grad.cpu(),
+           "lse": torch.zeros(1, 2, 300)}
+    for h in range(2):
+        qh, kh, vh, dOh = (_f64(x[n][0, h]) for n in ("q", "k", "v", "dO"))
+        o_ref, _ = oracle.attention_forward(qh, kh, vh, True, 64 ** -0.5)
+        check_tensor("O", _f64(out["o"][0, h]), o_ref)
+        dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward(qh, kh, vh, dOh, True, 64 ** -0.5)
+        check_tensor("dQ", _f64(out["dq"][0, h]), dq_ref)
+        check_tensor("dK", _f64(out["dk"][0, h]), dk_ref)
+        check_tensor("dV", _f64(out["dv"][0, h]), dv_ref)
 
 
 def test_workload_long_sequence():
