@@ -388,8 +388,13 @@ struct BwdCfg {
     static constexpr int B_DS = B_LD + 1;                   // P^T, dS^T written
     static constexpr int B_DQFULL = B_DS + 1;               // dQ in TMEM
     static constexpr int B_DQEMPTY = B_DQFULL + 1;          // dQ columns read out
-    static constexpr int B_STAGED = B_DQEMPTY + 1;          // dQ staged in smem
-    static constexpr int B_ACC = B_STAGED + 1;              // dV, dK final
+    // dQ staged in smem, one barrier per stage: phase k+1 of STAGED[s] needs
+    // stage s reloaded, hence released by the reducer after it saw phase k.
+    // (With a single barrier the compute warpgroups could stage two blocks
+    // while the reducer still finished the one before, and its parity wait
+    // would then miss both phases.)
+    static constexpr int B_STAGED = B_DQEMPTY + 1;          // [S]
+    static constexpr int B_ACC = B_STAGED + STAGES;         // dV, dK final
     static constexpr int B_DRAIN = B_ACC + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -462,7 +467,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar(C::B_DS), 256);
         mbar_init(bar(C::B_DQFULL), 1);
         mbar_init(bar(C::B_DQEMPTY), 256);
-        mbar_init(bar(C::B_STAGED), 256);
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(bar(C::B_STAGED + s), 256);
         mbar_init(bar(C::B_ACC), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
@@ -601,7 +606,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (lane == 0) {
                     for (int it = 0; it < n_it; ++it) {
                         const int s = it % C::STAGES;
-                        if (!wait_bar(wc, bar(C::B_STAGED), it & 1)) break;
+                        if (!wait_bar(wc, bar(C::B_STAGED + s), (it / C::STAGES) & 1)) break;
                         fence_proxy_async_smem();
         #pragma unroll
                         for (int b = 0; b < D / C::DQ_BOX_COLS; ++b)
@@ -752,7 +757,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                            q32[32 * h + 4 * k + 2], q32[32 * h + 4 * k + 3]);
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(bar(C::B_STAGED));
+                    mbar_arrive(bar(C::B_STAGED + s));
                 }
                 // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
                 if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));

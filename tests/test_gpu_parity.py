@@ -249,3 +249,22 @@ def test_repeated_calls_are_stable():
             assert torch.isfinite(out["o"].float()).all() and torch.isfinite(out["lse"]).all()
         for name in ("o", "lse", "dk", "dv"):
             assert torch.equal(out[name], first[name]), name
+
+
+def test_many_ctas_no_barrier_overrun():
+    """4096 CTAs with 1..32 query blocks each, run repeatedly with the device
+    status checked after every call.  Guards the backward's barrier protocol:
+    a barrier whose producer can complete two phases before its consumer
+    looks makes the consumer's parity wait run out, which shows up here as a
+    timeout status in a sizeable share of calls."""
+    w = WORKLOADS["fwdbwd_causal_b4_h32_n4096_d128"]
+    dev = torch.device("cuda:0")
+    x = {k: v.to(dev) for k, v in make_inputs(w.B, w.H, w.N, w.d, w.seed).items()}
+    o, lse, o32 = attn.forward(x["q"], x["k"], x["v"], True, w.scale, o32=True)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    bufs = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]))
+    for rep in range(30):
+        attn.backward(x["q"], x["k"], x["v"], o, lse, x["dO"], True, w.scale, o32=o32, **bufs)
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_status() == 0, "call %d" % rep
