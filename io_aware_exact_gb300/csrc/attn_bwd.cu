@@ -352,18 +352,27 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_o32_kernel(const PreO
 // blocks i that can see block j and keeps dV_j, dK_j in TMEM.  Per block i:
 //
 //   MMA:   S^T = K Q_i^T, dP^T = V dO_i^T                     (N = 128)
-//   WG0/1: P^T = exp2(S^T tau log2e - lse2), dS^T = P^T (dP^T - D), for
-//          query columns [64c, 64c + 64) each; P^T and dS^T go back into
-//          TMEM as 16-bit pairs and dS^T also into shared memory
-//   MMA:   dV += P^T dO_i, dK += dS^T Q_i (A from TMEM), dQ = dS K_j
+//   WG0/1: P^T = exp2(S^T tau log2e - lse2) for query columns [64c, 64c+64),
+//          back into TMEM as 16-bit pairs over the first half of the same
+//          columns; later dS^T = P^T (dP^T - D), into TMEM over the first half
+//          of the dP^T columns and into shared memory
+//   MMA:   dV += P^T dO_i as soon as P^T is in, dK += dS^T Q_i (A from TMEM),
+//          dQ = dS K_j
 //   WG0/1: dQ rows read out of TMEM, staged in shared memory over the Q_i /
 //          dO_i tiles (no longer read by then); warp 2 adds them to dq_accum
 //          with TMA tensor reduce-adds and hands the stage back to the TMA
 //          producer.
 //
-// TMEM columns: S^T at 0 (then P^T at 0 and dS^T at 64, packed), dP^T at 128
-// (then dQ at 128, d columns), dV at 256, dK at 256 + d.  The next block's
-// S^T is issued right after dQ; its dP^T waits until dQ has been read out.
+// Overlap: the tensor core runs S^T_i, dP^T_i, dV_i, dK_i, dQ_i in that order
+// with one barrier per product, so the exponentials of block i overlap dP^T_i
+// and the dS_i arithmetic overlaps dV_i.  (Issuing S^T_{i+1} before dQ_i
+// would make it wait for the next Q tile, whose stage is only freed once the
+// dQ of the block before has been reduced.)
+//
+// TMEM columns: S^T at 0 (P^T of warpgroup c at 64c, 32 packed columns),
+// dP^T at 128 (dS^T of warpgroup c at 128 + 64c; then dQ at 128, d columns),
+// dV at 256, dK at 256 + d.  Each warpgroup only overwrites columns it has
+// read itself.  dP^T_{i+1} waits until dQ_i has been read out.
 template <int D>
 struct BwdCfg {
     static constexpr int STAGES = (D == 128) ? 2 : 3;       // Q_i / dO_i ring depth
@@ -383,9 +392,10 @@ struct BwdCfg {
     static constexpr int B_QEMPTY = B_DOFULL + STAGES;      // stage free (after dQ reduce read)
     static constexpr int B_STFULL = B_QEMPTY + STAGES;      // stats ready  [S]
     static constexpr int B_STEMPTY = B_STFULL + STAGES;     // stats free   [S]
-    static constexpr int B_SDP = B_STEMPTY + STAGES;        // S^T, dP^T in TMEM
-    static constexpr int B_LD = B_SDP + 1;                  // both warpgroups read S^T, dP^T
-    static constexpr int B_DS = B_LD + 1;                   // P^T, dS^T written
+    static constexpr int B_SFULL = B_STEMPTY + STAGES;      // S^T in TMEM
+    static constexpr int B_DPFULL = B_SFULL + 1;            // dP^T in TMEM
+    static constexpr int B_PREADY = B_DPFULL + 1;           // P^T written (S^T read)
+    static constexpr int B_DS = B_PREADY + 1;               // dS^T written (dP^T read)
     static constexpr int B_DQFULL = B_DS + 1;               // dQ in TMEM
     static constexpr int B_DQEMPTY = B_DQFULL + 1;          // dQ columns read out
     // dQ staged in smem, one barrier per stage: phase k+1 of STAGED[s] needs
@@ -404,7 +414,7 @@ struct BwdCfg {
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + SLACK;
     static constexpr int THREADS = 384;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = 0, P_COL = 0, DS_COL = 64, DP_COL = 128, DQ_COL = 128;
+    static constexpr uint32_t S_COL = 0, P_COL = 0, DP_COL = 128, DS_COL = 128, DQ_COL = 128;
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
     static constexpr int DQ_BOX_COLS = 32;                  // fp32 columns per reduce box
     static constexpr int DQ_BOX_BYTES = kTile * DQ_BOX_COLS * 4;   // 16 KB
@@ -462,8 +472,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(C::B_STFULL + s), 32);
             mbar_init(bar(C::B_STEMPTY + s), 256);
         }
-        mbar_init(bar(C::B_SDP), 1);
-        mbar_init(bar(C::B_LD), 256);
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_DPFULL), 1);
+        mbar_init(bar(C::B_PREADY), 256);
         mbar_init(bar(C::B_DS), 256);
         mbar_init(bar(C::B_DQFULL), 1);
         mbar_init(bar(C::B_DQEMPTY), 256);
@@ -545,16 +556,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     constexpr uint32_t id_kk = idesc_f16(128, 128, fmt, 0, 0);  // K x Q^T, V x dO^T
                     constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
                     constexpr uint32_t id_dq = idesc_f16(128, D, fmt, 1, 1);    // dS x K (both MN-major)
-                    bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
-                    for (int it = 0; ok && it < n_it; ++it) {
-                        const int s = it % C::STAGES;
-                        const uint32_t ph = (it / C::STAGES) & 1;
-                        const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
-                        const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
-                        if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
-                        tc_fence_after();
-                        // S^T = K Q^T   (P^T and dS^T of the previous block were consumed by
-                        // the dV / dK MMAs issued before this one)
+                    // S^T = K Q_i^T into the S columns, committed to SFULL
+                    auto issue_s = [&](int it) {
+                        const uint32_t q_s = sbase + C::Q_OFF + (it % C::STAGES) * C::TILE_BYTES;
         #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -562,6 +566,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    smem_desc(sbase + C::K_OFF + off, 16, 1024, LAYOUT_SW128),
                                    smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
                         }
+                        mma_commit(bar(C::B_SFULL));
+                    };
+                    bool ok = wait_bar(wc, bar(C::B_KVFULL), 0);
+                    for (int it = 0; ok && it < n_it; ++it) {
+                        const int s = it % C::STAGES;
+                        const uint32_t ph = (it / C::STAGES) & 1;
+                        const uint32_t q_s = sbase + C::Q_OFF + s * C::TILE_BYTES;
+                        const uint32_t do_s = sbase + C::DO_OFF + s * C::TILE_BYTES;
+                        // S^T of this block: the previous P^T was consumed by its dV MMA
+                        if (!(ok = wait_bar(wc, bar(C::B_QFULL + s), ph))) break;
+                        tc_fence_after();
+                        issue_s(it);
                         if (!(ok = wait_bar(wc, bar(C::B_DOFULL + s), ph))) break;
                         // dP^T overwrites the previous block's dQ: wait for its readout
                         if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
@@ -574,18 +590,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    smem_desc(sbase + C::V_OFF + off, 16, 1024, LAYOUT_SW128),
                                    smem_desc(do_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
                         }
-                        mma_commit(bar(C::B_SDP));
-                        if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
+                        mma_commit(bar(C::B_DPFULL));
+                        // dV += P^T dO   (K = the 128 queries of block i; query step kk
+                        // lives with warpgroup kk / 4)
+                        if (!(ok = wait_bar(wc, bar(C::B_PREADY), it & 1))) break;
                         tc_fence_after();
-                        // dV += P^T dO ; dK += dS^T Q   (K = the 128 queries of block i)
         #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8,
+                            mma_ts(tmem + C::DV_COL, tmem + C::P_COL + 64 * (kk >> 2) + 8 * (kk & 3),
                                    smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
                                    (it > 0 || kk > 0) ? 1u : 0u);
+                        // dK += dS^T Q
+                        if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
+                        tc_fence_after();
         #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8,
+                            mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + 64 * (kk >> 2) + 8 * (kk & 3),
                                    smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
                                    (it > 0 || kk > 0) ? 1u : 0u);
                         // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
@@ -652,46 +672,37 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int key = j * kTile + r;
                 const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
                 const float cs = args.scale_log2;
+                const uint64_t cs2 = f2_pack(cs, cs);
                 const bool key_ok = key < N;
-                bool ok = true;
-                for (int it = 0; it < n_it; ++it) {
+                uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
+                float pv[64];        // P^T of this key row, query columns [64c, 64c + 64), fp32
+                // P^T_i: wait for S^T_i and block i's statistics, write packed P^T to TMEM
+                auto compute_p = [&](int it) -> bool {
                     const int s = it % C::STAGES;
                     const int i = i_start + it;
-                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SDP), it & 1) &&
-                                                     wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1));
-                    if (!ok) break;
+                    if (!__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL), it & 1) &&
+                                                     wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1)))
+                        return false;
                     tc_fence_after();
-                    // per query: -lse*log2e and -D (the loader stores both negated)
+                    // per query: -lse*log2e (the loader stores it negated)
                     const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
-                    const float4* dvv = reinterpret_cast<const float4*>(stats + s * 2 * kTile + kTile + 64 * c);
                     const int qbase = i * kTile + 64 * c;
                     // masking is needed only for keys past N and on the diagonal block
                     const bool masked = !key_ok || (CAUSAL && i == j);
-                    uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
-                    const uint64_t cs2 = f2_pack(cs, cs);
-                    uint32_t pp[32], pd[32];
-                    // two chunks of 32 query columns keep ~64 inputs live instead of 128
+                    uint32_t pp[32];
+                    // two chunks of 32 query columns keep 32 S values live at a time
         #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         // masked columns of this chunk are those below lim (the query
                         // precedes the key; all of them past the key tail)
                         const int lim = key_ok ? key - (qbase + 32 * ch) : 32;
-                        uint32_t sr[32], dr[32];
+                        uint32_t sr[32];
                         tmem_ld32(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
-                        tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32 * ch, dr);
                         tmem_ld_wait();
-                        if (ch == 1) {
-                            // P^T / dS^T overwrite S^T columns the other warpgroup reads:
-                            // both must have loaded them first
-                            tc_fence_before();
-                            mbar_arrive(bar(C::B_LD));
-                        }
         #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
                             const float4 nl = l2[8 * ch + e4];      // broadcast loads
-                            const float4 nd = dvv[8 * ch + e4];
                             const uint64_t nl2[2] = {f2_pack(nl.x, nl.y), f2_pack(nl.z, nl.w)};
-                            const uint64_t nd2[2] = {f2_pack(nd.x, nd.y), f2_pack(nd.z, nd.w)};
         #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int q = 4 * e4 + 2 * u;        // column within the chunk
@@ -705,24 +716,52 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                     if (q < lim) p0 = 0.f;
                                     if (q + 1 < lim) p1 = 0.f;
                                 }
-                                // dS = P (dP - D)
-                                const uint64_t dsv = f2_mul(f2_pack(p0, p1),
+                                pv[32 * ch + q] = p0;
+                                pv[32 * ch + q + 1] = p1;
+                                pp[16 * ch + 2 * e4 + u] = pack2<BF16>(p0, p1);
+                            }
+                        }
+                    }
+                    // over columns [64c, 64c + 32): read above by this thread only
+                    tmem_st32(tmem + lane_off + C::P_COL + 64 * c, pp);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_PREADY));
+                    return true;
+                };
+                // dS^T_i = P^T (dP^T - D): TMEM (for dK) and shared memory (for dQ)
+                auto compute_ds = [&](int it) -> bool {
+                    const int s = it % C::STAGES;
+                    if (!__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DPFULL), it & 1))) return false;
+                    tc_fence_after();
+                    const float4* dvv = reinterpret_cast<const float4*>(stats + s * 2 * kTile + kTile + 64 * c);
+                    uint32_t pd[32];
+        #pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t dr[32];
+                        tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32 * ch, dr);
+                        tmem_ld_wait();
+        #pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 nd = dvv[8 * ch + e4];      // -D, broadcast loads
+                            const uint64_t nd2[2] = {f2_pack(nd.x, nd.y), f2_pack(nd.z, nd.w)};
+        #pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int q = 4 * e4 + 2 * u;
+                                const uint64_t dsv = f2_mul(f2_pack(pv[32 * ch + q], pv[32 * ch + q + 1]),
                                                             f2_add(f2_pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1])),
                                                                    nd2[u]));
                                 float d0, d1;
                                 f2_unpack(dsv, d0, d1);
-                                pp[16 * ch + 2 * e4 + u] = pack2<BF16>(p0, p1);
                                 pd[16 * ch + 2 * e4 + u] = pack2<BF16>(d0, d1);
                             }
                         }
                     }
-                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_LD), it & 1));
-                    if (!ok) break;
-                    tc_fence_after();
-                    tmem_st32(tmem + lane_off + C::P_COL + 32 * c, pp);
-                    tmem_st32(tmem + lane_off + C::DS_COL + 32 * c, pd);
+                    // over dP^T columns [64c, 64c + 32): read above by this thread only
+                    tmem_st32(tmem + lane_off + C::DS_COL + 64 * c, pd);
                     // dS^T row -> shared memory, 128-byte swizzle: 16-byte chunk k of row
-                    // r sits at chunk position k ^ (r % 8)
+                    // r sits at chunk position k ^ (r % 8).  dQ of the previous block,
+                    // the last reader of this buffer, completed before its readout.
         #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         *reinterpret_cast<uint4*>(ds_row + ((k ^ (r & 7)) * 16)) =
@@ -732,9 +771,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_before();
                     mbar_arrive(bar(C::B_DS));
                     mbar_arrive(bar(C::B_STEMPTY + s));
-                    // dQ_i readout (lane = query row of block i) and staging for the reducer
-                    ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1));
-                    if (!ok) break;
+                    return true;
+                };
+                // dQ_i readout (lane = query row of block i) and staging for the reducer
+                auto readout_dq = [&](int it) -> bool {
+                    const int s = it % C::STAGES;
+                    if (!__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_DQFULL), it & 1))) return false;
                     tc_fence_after();
                     constexpr int NQ = D / 2;                 // dQ columns per warpgroup
                     uint32_t q32[NQ];
@@ -758,7 +800,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(bar(C::B_STAGED + s));
-                }
+                    return true;
+                };
+                bool ok = true;
+                for (int it = 0; ok && it < n_it; ++it)
+                    ok = compute_p(it) && compute_ds(it) && readout_dq(it);
                 // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
                 if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
                 if (ok) {
