@@ -389,8 +389,9 @@ struct BwdCfg {
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_DOFULL = B_QFULL + STAGES;
-    static constexpr int B_QEMPTY = B_DOFULL + STAGES;      // stage free (after dQ reduce read)
-    static constexpr int B_STFULL = B_QEMPTY + STAGES;      // stats ready  [S]
+    static constexpr int B_QEMPTY = B_DOFULL + STAGES;      // Q_i tile free (its dQ boxes reduced)
+    static constexpr int B_DOEMPTY = B_QEMPTY + STAGES;     // dO_i tile free (its dQ boxes reduced)
+    static constexpr int B_STFULL = B_DOEMPTY + STAGES;     // stats ready  [S]
     static constexpr int B_STEMPTY = B_STFULL + STAGES;     // stats free   [S]
     static constexpr int B_SFULL = B_STEMPTY + STAGES;      // S^T in TMEM
     static constexpr int B_DPFULL = B_SFULL + 1;            // dP^T in TMEM
@@ -469,6 +470,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(C::B_QFULL + s), 1);
             mbar_init(bar(C::B_DOFULL + s), 1);
             mbar_init(bar(C::B_QEMPTY + s), 1);
+            mbar_init(bar(C::B_DOEMPTY + s), 1);
             mbar_init(bar(C::B_STFULL + s), 32);
             mbar_init(bar(C::B_STEMPTY + s), 256);
         }
@@ -521,11 +523,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
                                     j * kTile, bh, pol_kv);
                     }
-                    int issued = 0;
+                    int issued_q = 0, issued_do = 0;   // tiles whose loads were issued
                     bool ok = true;
                     for (int it = 0; it < n_it; ++it) {
                         const int s = it % C::STAGES;
                         const int i = i_start + it;
+                        // the two tiles of a stage are released separately: the dQ
+                        // boxes staged over Q_i are reduced first
                         if (it >= C::STAGES) {
                             ok = wait_bar(wc, bar(C::B_QEMPTY + s), ((it / C::STAGES) - 1) & 1);
                             if (!ok) break;
@@ -534,19 +538,23 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int b = 0; b < C::KBOX; ++b)
                             tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
                                         bar(C::B_QFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
+                        issued_q = it + 1;
+                        if (it >= C::STAGES) {
+                            ok = wait_bar(wc, bar(C::B_DOEMPTY + s), ((it / C::STAGES) - 1) & 1);
+                            if (!ok) break;
+                        }
                         mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
                             tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
                                         bar(C::B_DOFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
-                        issued = it + 1;
+                        issued_do = it + 1;
                     }
                     if (!ok) {
                         drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
-                        for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
-                            const int s = it % C::STAGES;
-                            drain_wait(bar(C::B_QFULL + s), (it / C::STAGES) & 1, 1000000000ull);
-                            drain_wait(bar(C::B_DOFULL + s), (it / C::STAGES) & 1, 1000000000ull);
-                        }
+                        for (int it = max(0, issued_q - C::STAGES); it < issued_q; ++it)
+                            drain_wait(bar(C::B_QFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
+                        for (int it = max(0, issued_do - C::STAGES); it < issued_do; ++it)
+                            drain_wait(bar(C::B_DOFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
                     }
                 }
             } else if (warp == 1) {
@@ -628,13 +636,23 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const int s = it % C::STAGES;
                         if (!wait_bar(wc, bar(C::B_STAGED + s), (it / C::STAGES) & 1)) break;
                         fence_proxy_async_smem();
+                        // boxes staged over Q_i first: the next Q tile is needed first
+                        constexpr int NB = D / C::DQ_BOX_COLS;
+                        constexpr int NB_Q = C::TILE_BYTES / C::DQ_BOX_BYTES;   // boxes over Q_i
         #pragma unroll
-                        for (int b = 0; b < D / C::DQ_BOX_COLS; ++b)
+                        for (int b = 0; b < NB_Q; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
                                               (i_start + it) * kTile, bh);
                         bulk_commit_group();
-                        bulk_wait_group_read0();
+        #pragma unroll
+                        for (int b = NB_Q; b < NB; ++b)
+                            tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
+                                              (i_start + it) * kTile, bh);
+                        bulk_commit_group();
+                        bulk_wait_group_read<1>();
                         mbar_arrive(bar(C::B_QEMPTY + s));
+                        bulk_wait_group_read<0>();
+                        mbar_arrive(bar(C::B_DOEMPTY + s));
                     }
                     bulk_wait_group0();
                 }
