@@ -11,7 +11,8 @@ forward 4*B*H*N^2*d, forward+backward 10*B*H*N^2*d, each halved for causal.
 
 Prints ONE JSON line on rank 0.  The reference arm (--impl reference) times
 the fp64 CPU oracle, as it stands, on the host cores over a bounded sample
-of the same workload (whole heads).
+of the same workload (256 query rows and 256 key columns of one head per
+step).
 """
 from __future__ import annotations
 
