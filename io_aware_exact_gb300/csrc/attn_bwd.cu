@@ -389,9 +389,7 @@ struct BwdCfg {
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_DOFULL = B_QFULL + STAGES;
-    static constexpr int B_QEMPTY = B_DOFULL + STAGES;      // Q_i tile free (its dQ boxes reduced)
-    static constexpr int B_DOEMPTY = B_QEMPTY + STAGES;     // dO_i tile free (its dQ boxes reduced)
-    static constexpr int B_STFULL = B_DOEMPTY + STAGES;     // stats ready  [S]
+    static constexpr int B_STFULL = B_DOFULL + STAGES;      // stats ready  [S]
     static constexpr int B_STEMPTY = B_STFULL + STAGES;     // stats free   [S]
     static constexpr int B_SFULL = B_STEMPTY + STAGES;      // S^T in TMEM
     static constexpr int B_DPFULL = B_SFULL + 1;            // dP^T in TMEM
@@ -469,8 +467,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar(C::B_QFULL + s), 1);
             mbar_init(bar(C::B_DOFULL + s), 1);
-            mbar_init(bar(C::B_QEMPTY + s), 1);
-            mbar_init(bar(C::B_DOEMPTY + s), 1);
             mbar_init(bar(C::B_STFULL + s), 32);
             mbar_init(bar(C::B_STEMPTY + s), 256);
         }
@@ -523,38 +519,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
                                     j * kTile, bh, pol_kv);
                     }
-                    int issued_q = 0, issued_do = 0;   // tiles whose loads were issued
-                    bool ok = true;
-                    for (int it = 0; it < n_it; ++it) {
-                        const int s = it % C::STAGES;
+                    // Only the first STAGES Q / dO tiles: the dQ reducer reloads each
+                    // stage itself as soon as its reductions have read it (see there).
+                    for (int it = 0; it < min(n_it, C::STAGES); ++it) {
                         const int i = i_start + it;
-                        // the two tiles of a stage are released separately: the dQ
-                        // boxes staged over Q_i are reduced first
-                        if (it >= C::STAGES) {
-                            ok = wait_bar(wc, bar(C::B_QEMPTY + s), ((it / C::STAGES) - 1) & 1);
-                            if (!ok) break;
-                        }
-                        mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
+                        mbar_arrive_expect_tx(bar(C::B_QFULL + it), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
-                            tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                        bar(C::B_QFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
-                        issued_q = it + 1;
-                        if (it >= C::STAGES) {
-                            ok = wait_bar(wc, bar(C::B_DOEMPTY + s), ((it / C::STAGES) - 1) & 1);
-                            if (!ok) break;
-                        }
-                        mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
+                            tma_load_3d(sbase + C::Q_OFF + it * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                        bar(C::B_QFULL + it), b * kBoxCols, i * kTile, bh, pol_q);
+                        mbar_arrive_expect_tx(bar(C::B_DOFULL + it), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
-                            tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
-                                        bar(C::B_DOFULL + s), b * kBoxCols, i * kTile, bh, pol_q);
-                        issued_do = it + 1;
-                    }
-                    if (!ok) {
-                        drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
-                        for (int it = max(0, issued_q - C::STAGES); it < issued_q; ++it)
-                            drain_wait(bar(C::B_QFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
-                        for (int it = max(0, issued_do - C::STAGES); it < issued_do; ++it)
-                            drain_wait(bar(C::B_DOFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
+                            tma_load_3d(sbase + C::DO_OFF + it * C::TILE_BYTES + b * kBoxBytes, &tm_do,
+                                        bar(C::B_DOFULL + it), b * kBoxCols, i * kTile, bh, pol_q);
                     }
                 }
             } else if (warp == 1) {
@@ -631,30 +607,61 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             } else if (warp == 2) {
                 // ------------------------------------------------------------ dQ reducer
+                // Adds each staged dQ tile to dq_accum with TMA reduce-adds and then
+                // reloads the stage for block it + STAGES.  The reload of Q (needed
+                // first, by the next S^T) is issued between the reductions of the
+                // boxes staged over Q and those staged over dO: the SM's TMA engine
+                // works through its queue in order, so the load does not wait
+                // behind the second half of the reduction.
                 if (lane == 0) {
+                    const uint64_t pol_q = policy_evict_last();
+                    constexpr int NB = D / C::DQ_BOX_COLS;
+                    constexpr int NB_Q = C::TILE_BYTES / C::DQ_BOX_BYTES;   // boxes over Q_i
+                    int issued_q = 0, issued_do = 0;   // blocks whose reloads were issued
                     for (int it = 0; it < n_it; ++it) {
                         const int s = it % C::STAGES;
+                        const int nxt = it + C::STAGES;  // block that reuses this stage
                         if (!wait_bar(wc, bar(C::B_STAGED + s), (it / C::STAGES) & 1)) break;
                         fence_proxy_async_smem();
-                        // boxes staged over Q_i first: the next Q tile is needed first
-                        constexpr int NB = D / C::DQ_BOX_COLS;
-                        constexpr int NB_Q = C::TILE_BYTES / C::DQ_BOX_BYTES;   // boxes over Q_i
         #pragma unroll
                         for (int b = 0; b < NB_Q; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
                                               (i_start + it) * kTile, bh);
                         bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                        if (nxt < n_it) {
+                            mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
+                            for (int b = 0; b < C::KBOX; ++b)
+                                tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
+                                            bar(C::B_QFULL + s), b * kBoxCols, (i_start + nxt) * kTile, bh, pol_q);
+                            issued_q = nxt + 1;
+                        }
         #pragma unroll
                         for (int b = NB_Q; b < NB; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
                                               (i_start + it) * kTile, bh);
                         bulk_commit_group();
-                        bulk_wait_group_read<1>();
-                        mbar_arrive(bar(C::B_QEMPTY + s));
                         bulk_wait_group_read<0>();
-                        mbar_arrive(bar(C::B_DOEMPTY + s));
+                        if (nxt < n_it) {
+                            mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
+                            for (int b = 0; b < C::KBOX; ++b)
+                                tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
+                                            bar(C::B_DOFULL + s), b * kBoxCols, (i_start + nxt) * kTile, bh, pol_q);
+                            issued_do = nxt + 1;
+                        }
                     }
                     bulk_wait_group0();
+                    // Every load of this CTA must land before its shared memory goes
+                    // away, also when a role gave up early: wait (bounded, ignoring
+                    // the abort flag) for the last load issued into each stage and
+                    // for K / V.  On the normal path these phases completed long ago.
+                    const int total_q = max(issued_q, min(n_it, C::STAGES));
+                    const int total_do = max(issued_do, min(n_it, C::STAGES));
+                    drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
+                    for (int it = max(0, total_q - C::STAGES); it < total_q; ++it)
+                        drain_wait(bar(C::B_QFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
+                    for (int it = max(0, total_do - C::STAGES); it < total_do; ++it)
+                        drain_wait(bar(C::B_DOFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
                 }
             } else if (warp == 3) {
                 // ------------------------------------------------------------ lse / D loader
