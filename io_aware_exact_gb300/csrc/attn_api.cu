@@ -103,9 +103,9 @@ int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) 
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
 }
 
-// 3-D tensor map over the fp32 dQ accumulator [BH, N, d]: box = 32 columns
-// (128 bytes) x 128 rows x 1 head, 128-byte swizzle; rows beyond N of a head
-// are never written by a reduction through it.
+// 3-D tensor map over a contiguous [BH, N, d] fp32 array (the dQ accumulator,
+// the training forward's fp32 O): box = 32 columns (128 bytes) x 128 rows x
+// 1 head, 128-byte swizzle; rows beyond N of a head are never written through it.
 int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return ATTN_ERR_LAUNCH;
@@ -135,10 +135,16 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
     const int BH = B * H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to, to32;
     if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
-        (rc = make_map(&tv, v, BH, N, d, bf16)))
+        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&to, o, BH, N, d, bf16)))
         return rc;
+    // the plain forward never touches the fp32 map; it gets a copy of the O map
+    if (o32 != nullptr) {
+        if ((rc = make_map_f32(&to32, o32, BH, N, d))) return rc;
+    } else {
+        to32 = to;
+    }
     FwdArgs a{};
     a.o = o;
     a.o32 = o32;
@@ -149,7 +155,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
     a.scale_log2 = scale * kLog2e;
     a.timeout_ns = kDefaultTimeoutNs;
-    return map_launch(launch_fwd(tq, tk, tv, a, BH, d, causal != 0, bf16,
+    return map_launch(launch_fwd(tq, tk, tv, to, to32, a, BH, d, causal != 0, bf16,
                                  static_cast<cudaStream_t>(stream)));
 }
 

@@ -75,8 +75,8 @@ struct DqConvertArgs {
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, int BH, int d, bool causal, bool bf16,
-                       cudaStream_t stream);
+                       const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
+                       int d, bool causal, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int BH,
                        int d, bool causal, bool bf16, cudaStream_t stream);

@@ -51,7 +51,9 @@ struct FwdCfg {
     static constexpr int B_SFULL = B_KVEMPTY + STAGES;    // [2]
     static constexpr int B_PFULL = B_SFULL + 2;           // [2]
     static constexpr int B_OFULL = B_PFULL + 2;           // [2]
-    static constexpr int B_DRAIN = B_OFULL + 2;
+    static constexpr int B_EPI_STAGED = B_OFULL + 2;      // [2] epilogue round staged (128 arrivals)
+    static constexpr int B_EPI_FREE = B_EPI_STAGED + 2;   // [2] epilogue round read by the TMA store
+    static constexpr int B_DRAIN = B_EPI_FREE + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + runtime alignment slack
@@ -66,7 +68,8 @@ struct FwdCfg {
 template <int D, bool CAUSAL, bool BF16, bool TRAIN>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const __grid_constant__ CUtensorMap tm_o32, const FwdArgs args) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -103,6 +106,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(C::B_SFULL + t), 1);
             mbar_init(bar(C::B_PFULL + t), 128);
             mbar_init(bar(C::B_OFULL + t), 1);
+            mbar_init(bar(C::B_EPI_STAGED + t), 128);
+            mbar_init(bar(C::B_EPI_FREE + t), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
         // A failure recorded earlier on this device turns later CTAs into
@@ -114,6 +119,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
+        if (TRAIN) tma_prefetch_desc(&tm_o32);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -339,6 +346,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(bar(C::B_PFULL + t));
             }
             // ------------------------------------------------------------ epilogue
+            // O leaves through the tile's Q buffer (free once the tile's last MMA has
+            // completed) in rounds of one Q-tile size, written out with TMA tensor
+            // stores: the fp32 O in two rounds (TRAIN), then the 16-bit O.  Each
+            // thread stages its row in the 128-byte-swizzled box layout; the
+            // warpgroup's first thread issues the stores once all rows are in and
+            // hands the buffer back when the stores have read it.
             if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
             if (ok && nkv[t] > 0) {
                 tc_fence_after();
@@ -347,37 +360,72 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // rows (weights summing to 1) and rowsum(dO o O) matches the P the
                 // backward recomputes; lse keeps the exact sum either way.
                 const float inv_l = 1.0f / (TRAIN ? lb : l);
-                const bool valid = row < N;
-                using Vec = uint4;
-                Vec* dst = reinterpret_cast<Vec*>(static_cast<uint16_t*>(args.o) +
-                                                  (static_cast<size_t>(bh) * N + row) * D);
-                float4* dst32 = !TRAIN ? nullptr
-                                : reinterpret_cast<float4*>(args.o32 + (static_cast<size_t>(bh) * N + row) * D);
+                const bool issuer = (warp & 3) == 0 && lane == 0;
+                const uint32_t stage = sbase + C::Q_OFF + t * C::TILE_BYTES;
+                uint8_t* stage_row = smem + C::Q_OFF + t * C::TILE_BYTES + r * 128;
+                const int row0 = q0 + kTile * t;
+                constexpr int ROUNDS = TRAIN ? 3 : 1;
+                for (int k = 0; k < ROUNDS && ok; ++k) {
+                    const bool f32 = TRAIN && k < 2;
+                    if (k > 0) {
+                        ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_EPI_FREE + t), (k - 1) & 1));
+                        if (!ok) break;
+                    }
+                    if (f32) {
+                        // columns [k D/2, (k+1) D/2): boxes of 32 fp32 columns
     #pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t orr[32];
-                    tmem_ld32(o_addr + c, orr);
-                    tmem_ld_wait();
+                        for (int c = 0; c < D / 2; c += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(o_addr + k * (D / 2) + c, orr);
+                            tmem_ld_wait();
+                            uint8_t* box_row = stage_row + (c / 32) * kBoxBytes;
     #pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * inv_l);
-                    uint32_t pk[16];
+                            for (int ch = 0; ch < 8; ++ch)
+                                *reinterpret_cast<float4*>(box_row + ((ch ^ (r & 7)) * 16)) =
+                                    make_float4(__uint_as_float(orr[4 * ch]) * inv_l,
+                                                __uint_as_float(orr[4 * ch + 1]) * inv_l,
+                                                __uint_as_float(orr[4 * ch + 2]) * inv_l,
+                                                __uint_as_float(orr[4 * ch + 3]) * inv_l);
+                        }
+                    } else {
+                        // all D columns: boxes of 64 16-bit columns
     #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1]));
-                    if (valid) {
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(o_addr + c, orr);
+                            tmem_ld_wait();
+                            uint32_t pk[16];
     #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[c / 8 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                         pk[4 * v4 + 3]);
-                        if constexpr (TRAIN) {
+                            for (int e = 0; e < 16; ++e)
+                                pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                                    __uint_as_float(orr[2 * e + 1]) * inv_l);
+                            uint8_t* box_row = stage_row + (c / 64) * kBoxBytes;
+                            const int ch0 = (c % 64) / 8;   // 16-byte chunks of this 32-column piece
     #pragma unroll
-                            for (int v4 = 0; v4 < 8; ++v4)
-                                dst32[c / 4 + v4] = make_float4(__uint_as_float(orr[4 * v4]), __uint_as_float(orr[4 * v4 + 1]),
-                                                                __uint_as_float(orr[4 * v4 + 2]), __uint_as_float(orr[4 * v4 + 3]));
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
+                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::B_EPI_STAGED + t));
+                    if (issuer) {
+                        if (wait_bar(wc, bar(C::B_EPI_STAGED + t), k & 1)) {
+                            if (f32) {
+                                for (int b = 0; b < D / 64; ++b)
+                                    tma_store_3d(&tm_o32, stage + b * kBoxBytes, k * (D / 2) + 32 * b, row0, bh);
+                            } else {
+                                for (int b = 0; b < D / 64; ++b)
+                                    tma_store_3d(&tm_o, stage + b * kBoxBytes, 64 * b, row0, bh);
+                            }
+                            bulk_commit_group();
+                            bulk_wait_group_read<0>();
+                            mbar_arrive(bar(C::B_EPI_FREE + t));
                         }
                     }
                 }
-                if (valid)
+                if (issuer) bulk_wait_group0();
+                if (row < N)
                     args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
             }
         }
@@ -393,7 +441,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, bool CAUSAL, bool BF16, bool TRAIN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const FwdArgs& a, int BH,
+                                const CUtensorMap& tv, const CUtensorMap& to,
+                                const CUtensorMap& to32, const FwdArgs& a, int BH,
                                 cudaStream_t stream) {
     using C = FwdCfg<D>;
     auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN>;
@@ -401,17 +450,17 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid = lpt_grid(a.num_qblocks, BH);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, to32, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, int BH, int d, bool causal, bool bf16,
-                       cudaStream_t stream) {
+                       const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
+                       int d, bool causal, bool bf16, cudaStream_t stream) {
 #define ATTN_FWD_CASE(D_, C_, B_) \
     if (d == D_ && causal == C_ && bf16 == B_)                                  \
-        return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true>(tq, tk, tv, a, BH, stream) \
-                                : launch_fwd_t<D_, C_, B_, false>(tq, tk, tv, a, BH, stream);
+        return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true>(tq, tk, tv, to, to32, a, BH, stream) \
+                                : launch_fwd_t<D_, C_, B_, false>(tq, tk, tv, to, to32, a, BH, stream);
     ATTN_FWD_CASE(64, false, true)
     ATTN_FWD_CASE(64, true, true)
     ATTN_FWD_CASE(128, false, true)
