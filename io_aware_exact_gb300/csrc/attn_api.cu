@@ -227,8 +227,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
         (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
         return rc;
-    CUtensorMap tdq;
-    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d))) return rc;
+    CUtensorMap tdq, tdk, tdv;
+    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d)) || (rc = make_map(&tdk, dk, BH, N, d, bf16)) ||
+        (rc = make_map(&tdv, dv, BH, N, d, bf16)))
+        return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     BwdArgs a{};
     a.lse = lse;
@@ -243,7 +245,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.timeout_ns = kDefaultTimeoutNs;
-    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, a, BH, d, causal != 0, bf16, st))))
+    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, d, causal != 0, bf16, st))))
         return rc;
     DqConvertArgs c{};
     c.dq_accum = dq_accum;

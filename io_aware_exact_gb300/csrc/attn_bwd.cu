@@ -404,7 +404,8 @@ struct BwdCfg {
     // would then miss both phases.)
     static constexpr int B_STAGED = B_DQEMPTY + 1;          // [S]
     static constexpr int B_ACC = B_STAGED + STAGES;         // dV, dK final
-    static constexpr int B_DRAIN = B_ACC + 1;
+    static constexpr int B_EPI = B_ACC + 1;                 // [2] dV / dK rows staged (128 each)
+    static constexpr int B_DRAIN = B_EPI + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     // The d=128 layout needs (almost) all 227 KB, so it relies on the dynamic
@@ -435,7 +436,8 @@ template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
+                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                const __grid_constant__ CUtensorMap tm_dv, const BwdArgs args) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -478,6 +480,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar(C::B_DQEMPTY), 256);
         for (int s = 0; s < C::STAGES; ++s) mbar_init(bar(C::B_STAGED + s), 256);
         mbar_init(bar(C::B_ACC), 1);
+        mbar_init(bar(C::B_EPI + 0), 128);
+        mbar_init(bar(C::B_EPI + 1), 128);
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = (*reinterpret_cast<volatile int*>(args.status) != 0) ? 1 : 0;
         fence_barrier_init();
@@ -488,6 +492,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_dq);
+        tma_prefetch_desc(&tm_dk);
+        tma_prefetch_desc(&tm_dv);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -831,13 +837,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int it = 0; ok && it < n_it; ++it)
                     ok = compute_p(it) && compute_ds(it) && readout_dq(it);
                 // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
+                // Rounded rows are staged in the 128-byte-swizzled box layout over the
+                // V (dV) or K (dK) tile, no longer read once every MMA has completed,
+                // and written out with TMA tensor stores by the warpgroup's first thread.
                 if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
                 if (ok) {
                     tc_fence_after();
                     const float mul = (c == 0) ? 1.0f : args.scale;
                     const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
-                    uint16_t* out = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
-                                    (static_cast<size_t>(bh) * N + key) * D;
+                    const int region = (c == 0) ? C::V_OFF : C::K_OFF;
+                    uint8_t* stage_row = smem + region + r * 128;
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
@@ -848,12 +857,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 16; ++e)
                             pk[e] = pack2<BF16>(__uint_as_float(a32[2 * e]) * mul,
                                                 __uint_as_float(a32[2 * e + 1]) * mul);
-                        if (key < N) {
-                            uint4* dst = reinterpret_cast<uint4*>(out + cc);
+                        uint8_t* box_row = stage_row + (cc / 64) * kBoxBytes;
+                        const int ch0 = (cc % 64) / 8;
         #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4)
-                                dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                        }
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::B_EPI + c));
+                    if (wq == 0 && lane == 0 && wait_bar(wc, bar(C::B_EPI + c), 0)) {
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_store_3d(c == 0 ? &tm_dv : &tm_dk, sbase + region + b * kBoxBytes, 64 * b,
+                                         j * kTile, bh);
+                        bulk_commit_group();
+                        bulk_wait_group0();
                     }
                 }
         }
@@ -911,15 +929,15 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
 
 template <int D, bool CAUSAL, bool BF16>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                                int BH, cudaStream_t stream) {
+                                const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                                const CUtensorMap& tdv, const BwdArgs& a, int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid = lpt_grid(a.num_kvblocks, BH);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
     return cudaGetLastError();
 }
 
@@ -955,10 +973,12 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int BH,
-                       int d, bool causal, bool bf16, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
+                       bool bf16, cudaStream_t stream) {
 #define ATTN_BWD_CASE(D_, C_, B_) \
-    if (d == D_ && causal == C_ && bf16 == B_) return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, tdq, a, BH, stream);
+    if (d == D_ && causal == C_ && bf16 == B_) \
+        return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)
     ATTN_BWD_CASE(64, true, true)
     ATTN_BWD_CASE(128, false, true)

@@ -78,8 +78,9 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
                        int d, bool causal, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int BH,
-                       int d, bool causal, bool bf16, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
+                       bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const DsumArgs& a, int BH, int d, bool causal,
                             bool bf16, cudaStream_t stream);
