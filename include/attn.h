@@ -33,8 +33,10 @@
  *    legacy default stream) and returns without synchronising.  Argument
  *    errors are detected on the host before anything is enqueued.  A launch
  *    failure returns ATTN_ERR_LAUNCH.  Kernels never trap: a bounded wait that
- *    runs out records ATTN_ERR_TIMEOUT in the library's device status word,
- *    read with attn_get_device_status().
+ *    runs out (about 2 s of unsuccessful barrier polls; the bound counts
+ *    polls, so time the kernel spends preempted does not count) records
+ *    ATTN_ERR_TIMEOUT in the library's device status word, read with
+ *    attn_get_device_status().
  *  - Return value: an attn_status code (0 = success).  Nothing throws.
  */
 #ifndef IO_AWARE_EXACT_GB300_ATTN_H
@@ -180,9 +182,10 @@ int attn_get_device_status(void* stream);
 
 /*
  * Self-test of the failure path: launches one tiny kernel that waits on a
- * barrier nothing ever completes, with a wait limit of `timeout_us`
- * microseconds (1..1000000).  The kernel records ATTN_ERR_TIMEOUT and
- * returns; the GPU context stays usable.  Returns ATTN_OK once enqueued.
+ * barrier nothing ever completes, with a wait limit of about `timeout_us`
+ * microseconds (1..1000000; the limit is a number of barrier polls, about
+ * 2 us each).  The kernel records ATTN_ERR_TIMEOUT and returns; the GPU
+ * context stays usable.  Returns ATTN_OK once enqueued.
  */
 int attn_selftest_timeout(int timeout_us, void* stream);
 

@@ -19,7 +19,9 @@ __device__ int g_status;
 
 namespace {
 
-constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per CTA
+// try_wait polls before a bounded wait gives up: an unsuccessful poll suspends
+// the thread for about 2 us, so this is about 2 s.
+constexpr unsigned int kDefaultWaitPolls = 1000000u;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -154,7 +156,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.BH = BH;
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
     a.scale_log2 = scale * kLog2e;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_fwd(tq, tk, tv, to, to32, a, BH, d, causal != 0, bf16,
                                  static_cast<cudaStream_t>(stream)));
 }
@@ -184,7 +186,7 @@ int pre_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.N = N;
     a.BH = BH;
     a.scale_log2 = scale * kLog2e;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_bwd_preprocess(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -244,7 +246,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.num_kvblocks = (N + kTile - 1) / kTile;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.wait_polls = kDefaultWaitPolls;
     if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, d, causal != 0, bf16, st))))
         return rc;
     DqConvertArgs c{};
@@ -255,7 +257,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     return map_launch(launch_dq_convert(c, bf16, st));
 }
 
-__global__ void selftest_timeout_kernel(int* status, unsigned long long timeout_ns) {
+__global__ void selftest_timeout_kernel(int* status, unsigned int max_polls) {
     __shared__ __align__(8) uint64_t bar_storage;
     __shared__ int abort_flag;
     const uint32_t b = smem_u32(&bar_storage);
@@ -266,7 +268,7 @@ __global__ void selftest_timeout_kernel(int* status, unsigned long long timeout_
     }
     __syncthreads();
     // Nothing ever arrives on the barrier: the wait must run out and report.
-    const WaitCtx wc{&abort_flag, status, globaltimer_ns() + timeout_ns};
+    const WaitCtx wc{&abort_flag, status, max_polls};
     if (threadIdx.x == 0) (void)wait_bar(wc, b, 0);
 }
 
@@ -375,7 +377,7 @@ int attn_selftest_timeout(int timeout_us, void* stream) {
     int rc = current_device(&status);
     if (rc) return rc;
     selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        status, static_cast<unsigned long long>(timeout_us) * 1000ull);
+        status, static_cast<unsigned int>((timeout_us + 1) / 2));   // about 2 us per poll
     return map_launch(cudaGetLastError());
 }
 

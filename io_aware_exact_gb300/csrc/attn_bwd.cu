@@ -104,9 +104,9 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
     const int N = args.N;
     const int nblk = (N + kTile - 1) / kTile;
+    const int bh = blockIdx.x;
     if (grid_block() >= nblk) return;                               // padding CTA
     const int qi = nblk - 1 - grid_block();                         // heavy query blocks first
     const int nkv = CAUSAL ? min(nblk, qi + 1) : nblk;
@@ -141,7 +141,7 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const WaitCtx wc{abort_flag, args.status, args.wait_polls};
     const bool skip = *abort_flag != 0;
 
     if (!skip && warp >= 2) {
@@ -186,10 +186,10 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 issued = j + 1;
             }
             if (!ok) {
-                drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
+                drain_wait(bar(C::B_QFULL), 0);
                 for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-                    drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
-                    drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                    drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1);
+                    drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1);
                 }
             }
         }
@@ -227,7 +227,7 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mma_commit(bar(C::B_KVEMPTY + s));
             }
             mma_commit(bar(C::B_DRAIN));
-            drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+            drain_wait(bar(C::B_DRAIN), 0);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ row sums
@@ -248,13 +248,9 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // keys >= limit are masked: the key tail and, on the diagonal block, keys > row
             int limit = N - (j * kTile + 64 * c);
             if (CAUSAL) limit = min(limit, row - (j * kTile + 64 * c) + 1);
-            // all four loads in flight before one wait
+            // both loads in flight before one wait
             uint32_t sr[64], dr[64];
-            tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(tmem + lane_off + C::s_col(b) + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-            tmem_ld32(tmem + lane_off + C::dp_col(b) + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-            tmem_ld_wait();
+            tmem_ld_sync(tmem + lane_off + C::s_col(b) + 64 * c, sr, tmem + lane_off + C::dp_col(b) + 64 * c, dr);
             // the buffer can be refilled as soon as it has been read
             tc_fence_before();
             mbar_arrive(bar(C::B_FREE + b));
@@ -503,7 +499,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const WaitCtx wc{abort_flag, args.status, args.wait_polls};
     const bool skip = *abort_flag != 0;
 
     // Register budgets: 384 threads x 168 registers at launch; the role warps
@@ -609,7 +605,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     if (ok) mma_commit(bar(C::B_ACC));
                     mma_commit(bar(C::B_DRAIN));
-                    drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+                    drain_wait(bar(C::B_DRAIN), 0);
                 }
             } else if (warp == 2) {
                 // ------------------------------------------------------------ dQ reducer
@@ -663,11 +659,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // for K / V.  On the normal path these phases completed long ago.
                     const int total_q = max(issued_q, min(n_it, C::STAGES));
                     const int total_do = max(issued_do, min(n_it, C::STAGES));
-                    drain_wait(bar(C::B_KVFULL), 0, 1000000000ull);
+                    drain_wait(bar(C::B_KVFULL), 0);
                     for (int it = max(0, total_q - C::STAGES); it < total_q; ++it)
-                        drain_wait(bar(C::B_QFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
+                        drain_wait(bar(C::B_QFULL + it % C::STAGES), (it / C::STAGES) & 1);
                     for (int it = max(0, total_do - C::STAGES); it < total_do; ++it)
-                        drain_wait(bar(C::B_DOFULL + it % C::STAGES), (it / C::STAGES) & 1, 1000000000ull);
+                        drain_wait(bar(C::B_DOFULL + it % C::STAGES), (it / C::STAGES) & 1);
                 }
             } else if (warp == 3) {
                 // ------------------------------------------------------------ lse / D loader
@@ -728,8 +724,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // precedes the key; all of them past the key tail)
                         const int lim = key_ok ? key - (qbase + 32 * ch) : 32;
                         uint32_t sr[32];
-                        tmem_ld32(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
-                        tmem_ld_wait();
+                        tmem_ld_sync(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
         #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
                             const float4 nl = l2[8 * ch + e4];      // broadcast loads
@@ -770,8 +765,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         uint32_t dr[32];
-                        tmem_ld32(tmem + lane_off + C::DP_COL + 64 * c + 32 * ch, dr);
-                        tmem_ld_wait();
+                        tmem_ld_sync(tmem + lane_off + C::DP_COL + 64 * c + 32 * ch, dr);
         #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
                             const float4 nd = dvv[8 * ch + e4];      // -D, broadcast loads
@@ -811,11 +805,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     constexpr int NQ = D / 2;                 // dQ columns per warpgroup
                     uint32_t q32[NQ];
-        #pragma unroll
-                    for (int h = 0; h < NQ / 32; ++h)
-                        tmem_ld32(tmem + lane_off + C::DQ_COL + NQ * c + 32 * h,
-                                  *reinterpret_cast<uint32_t(*)[32]>(&q32[32 * h]));
-                    tmem_ld_wait();
+                    tmem_ld_sync(tmem + lane_off + C::DQ_COL + NQ * c, q32);
                     tc_fence_before();
                     mbar_arrive(bar(C::B_DQEMPTY));
                     // boxes of 32 fp32 columns, 128-byte swizzle: 16-byte chunk k of row r
@@ -850,8 +840,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
-                        tmem_ld32(tmem + lane_off + col + cc, a32);
-                        tmem_ld_wait();
+                        tmem_ld_sync(tmem + lane_off + col + cc, a32);
                         uint32_t pk[16];
         #pragma unroll
                         for (int e = 0; e < 16; ++e)
@@ -888,21 +877,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // ============================================================================
 // launchers
 // ============================================================================
-static int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 152;
-    }
-    return n;
-}
 
 cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream) {
     const long long rows_per_block = 256 / (a.d / 8);
     long long blocks = (a.rows + rows_per_block - 1) / rows_per_block;
-    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const long long cap = static_cast<long long>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (a.d == 64) {
@@ -919,7 +898,7 @@ cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream
 
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream) {
     long long blocks = (a.elems / 8 + 255) / 256;
-    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const long long cap = static_cast<long long>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (bf16) attn_dq_convert_kernel<true><<<blocks, 256, 0, stream>>>(a);

@@ -28,7 +28,7 @@ struct FwdArgs {
     int BH;                // batch * heads
     int num_qblocks;       // ceil(N / 256): CTAs per head
     float scale_log2;      // softmax scale * log2(e)
-    unsigned long long timeout_ns;
+    unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
 
 struct BwdArgs {
@@ -43,7 +43,7 @@ struct BwdArgs {
     int num_kvblocks;      // ceil(N / 128)
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
-    unsigned long long timeout_ns;
+    unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
 
 struct DsumArgs {
@@ -54,7 +54,7 @@ struct DsumArgs {
     int N;
     int BH;                // batch * heads
     float scale_log2;      // tau * log2(e)
-    unsigned long long timeout_ns;
+    unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
 
 struct PreO32Args {
@@ -89,9 +89,10 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
 
 // Grid layout shared by the attention kernels: x = (batch, head), y/z = block
 // index within a head.  Launch order is x fastest, so every head's heaviest
-// causal block is scheduled before any lighter one (longest work first; a
-// head-major order, tried as well, left a tail of heavy blocks of the last
-// heads).  y is capped at the hardware limit and z extends it.
+// causal block is scheduled before any lighter one (longest work first).  y
+// is capped at the hardware limit and z extends it.  The index math is two
+// reads of blockIdx: the backward runs at its register limit, and a head order
+// in groups, computed with divisions in the kernel, cost it about 4%.
 constexpr int kMaxGridY = 65535;
 
 inline dim3 lpt_grid(int blocks_per_head, int BH) {
@@ -103,6 +104,17 @@ inline dim3 lpt_grid(int blocks_per_head, int BH) {
 // for padding CTAs of the last z-slice.
 __device__ __forceinline__ int grid_block() {
     return static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
+}
+
+inline int device_sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 152;
+    }
+    return n;
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -130,7 +130,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtx wc{abort_flag, args.status, globaltimer_ns() + args.timeout_ns};
+    const WaitCtx wc{abort_flag, args.status, args.wait_polls};
     const bool skip = *abort_flag != 0;
 
     if (warp < 4) {
@@ -167,10 +167,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (!ok) {
                     // let copies already in flight land before the CTA's smem goes away
-                    drain_wait(bar(C::B_QFULL), 0, 1000000000ull);
+                    drain_wait(bar(C::B_QFULL), 0);
                     for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-                        drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
-                        drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, 1000000000ull);
+                        drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1);
+                        drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1);
                     }
                 }
             }
@@ -236,7 +236,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 // make sure no MMA is still reading smem / writing TMEM at teardown
                 mma_commit(bar(C::B_DRAIN));
-                drain_wait(bar(C::B_DRAIN), 0, 1000000000ull);
+                drain_wait(bar(C::B_DRAIN), 0);
             }
         }
     } else {
@@ -258,13 +258,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[128];
-                tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-                tmem_ld_wait();
-                float* sv = reinterpret_cast<float*>(sr);
+                float sv[128];
+                tmem_ld_sync(s_addr, sv);
                 // mask: key tail (keys >= N) and, on the diagonal block, keys > row
                 int limit = N - j * kTile;
                 if (CAUSAL) limit = min(limit, row - j * kTile + 1);
@@ -333,8 +328,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         uint32_t orr[32];
-                        tmem_ld32(o_addr + c, orr);
-                        tmem_ld_wait();
+                        tmem_ld_sync(o_addr + c, orr);
     #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
@@ -376,8 +370,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     #pragma unroll
                         for (int c = 0; c < D / 2; c += 32) {
                             uint32_t orr[32];
-                            tmem_ld32(o_addr + k * (D / 2) + c, orr);
-                            tmem_ld_wait();
+                            tmem_ld_sync(o_addr + k * (D / 2) + c, orr);
                             uint8_t* box_row = stage_row + (c / 32) * kBoxBytes;
     #pragma unroll
                             for (int ch = 0; ch < 8; ++ch)
@@ -392,8 +385,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     #pragma unroll
                         for (int c = 0; c < D; c += 32) {
                             uint32_t orr[32];
-                            tmem_ld32(o_addr + c, orr);
-                            tmem_ld_wait();
+                            tmem_ld_sync(o_addr + c, orr);
                             uint32_t pk[16];
     #pragma unroll
                             for (int e = 0; e < 16; ++e)

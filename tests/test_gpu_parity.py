@@ -268,3 +268,37 @@ def test_many_ctas_no_barrier_overrun():
         attn.backward(x["q"], x["k"], x["v"], o, lse, x["dO"], True, w.scale, o32=o32, **bufs)
         torch.cuda.synchronize()
         assert attn.attn_get_device_status() == 0, "call %d" % rep
+
+
+def test_results_do_not_depend_on_the_clock():
+    """Calls spread over more than 2^32 ns (one wrap of the low word of the
+    GPU's nanosecond timer) all return the same bits as the first, for the
+    forward, the training forward and the backward.  A clock value kept live
+    in a kernel once leaked into the forward's softmax, so that about a
+    quarter of that cycle every row came out empty (lse = -inf, O = NaN)."""
+    import time
+    dev = torch.device("cuda:0")
+    B, H, N, d, scale = 1, 4, 1000, 128, 128 ** -0.5
+    x = {k: v.to(dev) for k, v in make_inputs(B, H, N, d, seed=300).items()}
+
+    def run():
+        o, lse = attn.forward(x["q"], x["k"], x["v"], True, scale)
+        o_t, lse_t, o32 = attn.forward(x["q"], x["k"], x["v"], True, scale, o32=True)
+        dq, dk, dv = attn.backward(x["q"], x["k"], x["v"], o_t, lse_t, x["dO"], True, scale, o32=o32)
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_status() == 0
+        return dict(o=o, lse=lse, o_t=o_t, lse_t=lse_t, dk=dk, dv=dv, dq=dq)
+
+    first = run()
+    for name, t in first.items():
+        assert torch.isfinite(t.float()).all(), name
+    t_end = time.monotonic() + 4.6
+    calls = 0
+    while time.monotonic() < t_end:
+        out = run()
+        calls += 1
+        for name in ("o", "lse", "o_t", "lse_t", "dk", "dv"):
+            assert torch.equal(out[name], first[name]), "%s differs at call %d" % (name, calls)
+        assert torch.isfinite(out["dq"].float()).all(), "dq at call %d" % calls
+        time.sleep(0.01)
+    assert calls > 100
