@@ -652,7 +652,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             issued_do = nxt + 1;
                         }
                     }
-                    bulk_wait_group0();
+                    bulk_wait_group_read<0>();   // shared memory read; the adds complete with the kernel
                     // Every load of this CTA must land before its shared memory goes
                     // away, also when a role gave up early: wait (bounded, ignoring
                     // the abort flag) for the last load issued into each stage and
@@ -860,7 +860,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             tma_store_3d(c == 0 ? &tm_dv : &tm_dk, sbase + region + b * kBoxBytes, 64 * b,
                                          j * kTile, bh);
                         bulk_commit_group();
-                        bulk_wait_group0();
+                        bulk_wait_group_read<0>();   // shared memory read; writes complete with the kernel
                     }
                 }
         }

@@ -292,8 +292,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint64_t cs2 = f2_pack(cs, cs);
                 const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t sum2 = f2_pack(0.f, 0.f);
-                uint64_t sumb2 = f2_pack(0.f, 0.f);
-                // TRAIN also sums the rounded p (one more unpack and add per pair);
+                float sumb0 = 0.f, sumb1 = 0.f;
+                // TRAIN also sums the rounded p (two widening adds per pair);
                 // it stores P in 16-column pieces (32 values) to keep that in registers.
                 constexpr int PW = TRAIN ? 32 : 64;  // p values per TMEM store
     #pragma unroll
@@ -308,7 +308,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const float p1 = ex2_approx(a1);
                         sum2 = f2_add(sum2, f2_pack(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
-                        if constexpr (TRAIN) sumb2 = f2_add(sumb2, unpack2_f2<BF16>(pk[e]));
+                        if constexpr (TRAIN) add_halves<BF16>(sumb0, sumb1, pk[e]);
                     }
                     if constexpr (TRAIN)
                         tmem_st16(s_addr + PW / 2 * h, pk);
@@ -318,10 +318,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float sum0, sum1;
                 f2_unpack(sum2, sum0, sum1);
                 l += sum0 + sum1;
-                if constexpr (TRAIN) {
-                    f2_unpack(sumb2, sum0, sum1);
-                    lb += sum0 + sum1;
-                }
+                if constexpr (TRAIN) lb += sumb0 + sumb1;
                 // Rescale O after the P stores, when the S registers are dead.  O holds
                 // P V up to block j-1 (S of block j was committed after that MMA).
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -416,7 +413,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     }
                 }
-                if (issuer) bulk_wait_group0();
+                // The stores only have to finish reading shared memory before the
+                // CTA exits (done above); their global writes complete with the
+                // kernel, and waiting for them here kept the next CTA off the SM.
                 if (row < N)
                     args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
             }
