@@ -165,3 +165,43 @@ def attention_backward(q, k, v, dO, causal: bool, scale: float):
     lse, D, dq = attention_backward_rows(q, k, v, dO, causal, scale)
     dk, dv = attention_backward_cols(q, k, v, dO, lse, D, causal, scale)
     return dq, dk, dv, lse, D
+
+
+def kv_head_of(h: int, H: int, Hkv: int) -> int:
+    """K / V head read by query head h when contiguous groups of H / Hkv query
+    heads share one K / V head (grouped-query attention; Hkv = 1 is
+    multi-query).  The paldyn.com survey lists GQA support among
+    FlashAttention-2's additions ("v1에서 v3까지") without defining it; this
+    is its plain reading."""
+    assert Hkv >= 1 and H % Hkv == 0
+    return h // (H // Hkv)
+
+
+def attention_forward_grouped(q, k, v, causal: bool, scale: float):
+    """O [H, nq, dv], lse [H, nq] for q [H, nq, d] and k, v [Hkv, nk, *]: each
+    query head is single-head attention with its group's K / V head."""
+    H, Hkv = len(q), len(k)
+    outs = [attention_forward(q[h], k[kv_head_of(h, H, Hkv)], v[kv_head_of(h, H, Hkv)],
+                              causal, scale) for h in range(H)]
+    return np.stack([o for o, _ in outs]), np.stack([l for _, l in outs])
+
+
+def attention_backward_grouped(q, k, v, dO, causal: bool, scale: float):
+    """(dQ [H], dK [Hkv], dV [Hkv], lse [H], D [H]) for grouped K / V heads.
+
+    dQ of a query head is the single-head dQ with its group's K / V.  K and V
+    of a group enter every query head of the group, so by the chain rule
+    their gradients are the sums of the single-head dK, dV over the group.
+    """
+    H, Hkv = len(q), len(k)
+    dq = np.zeros(np.shape(q), np.float64)
+    dk = np.zeros(np.shape(k), np.float64)
+    dv = np.zeros(np.shape(v), np.float64)
+    lse = np.zeros(np.shape(q)[:2], np.float64)
+    D = np.zeros(np.shape(q)[:2], np.float64)
+    for h in range(H):
+        g = kv_head_of(h, H, Hkv)
+        dq[h], dk_h, dv_h, lse[h], D[h] = attention_backward(q[h], k[g], v[g], dO[h], causal, scale)
+        dk[g] += dk_h
+        dv[g] += dv_h
+    return dq, dk, dv, lse, D

@@ -304,3 +304,38 @@ def test_backward_column_subset_matches_full():
     assert np.array_equal(dk2, dk[cols]) and np.array_equal(dv2, dvv[cols])
     lse3, D3, dq3 = oracle.attention_backward_rows(q, k, v, dO, True, 0.5, rows=[4, 9])
     assert np.array_equal(dq3, dq[[4, 9]]) and np.array_equal(D3, D[[4, 9]])
+
+
+# --------------------------------------------------------------------------
+# Grouped K / V heads
+# --------------------------------------------------------------------------
+
+def test_grouped_head_mapping_is_contiguous():
+    """Query heads 0..3 share K / V head 0 and 4..7 head 1 (H=8, Hkv=2); one
+    K / V head serves all (multi-query); Hkv = H is plain multi-head."""
+    assert [oracle.kv_head_of(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.kv_head_of(h, 3, 1) for h in range(3)] == [0, 0, 0]
+    assert [oracle.kv_head_of(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("H,Hkv,causal", [(4, 2, False), (4, 2, True), (3, 1, True)])
+def test_grouped_backward_matches_finite_differences(H, Hkv, causal):
+    """Central differences of L = sum over query heads of sum(dO_h * O_h)
+    w.r.t. every entry of the shared K and V (and of Q): a dK / dV that is
+    not summed over the group, or summed over the wrong heads, fails."""
+    r = _rng(40 + H + Hkv + int(causal))
+    n, d, dv, tau = 4, 3, 2, 0.7
+    q, dO = r.normal(size=(H, n, d)), r.normal(size=(H, n, dv))
+    k, v = r.normal(size=(Hkv, n, d)), r.normal(size=(Hkv, n, dv))
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward_grouped(qq, kk, vv, causal, tau)
+        return float(np.sum(o * dO))
+
+    dq, dk, dvv, _, _ = oracle.attention_backward_grouped(q, k, v, dO, causal, tau)
+    gq = _fd_grad(q, lambda x: loss(x, k, v))
+    gk = _fd_grad(k, lambda x: loss(q, x, v))
+    gv = _fd_grad(v, lambda x: loss(q, k, x))
+    for got, want in ((dq, gq), (dk, gk), (dvv, gv)):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
