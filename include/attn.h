@@ -170,6 +170,44 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* dO
                      const float* lse, void* dq, void* dk, void* dv,
                      int B, int H, int N, int d, int causal, float scale, void* stream);
 
+/*
+ * Grouped key / value heads (GQA; MQA when Hkv = 1).  The "v1에서 v3까지"
+ * version table of the paldyn.com survey ("어텐션 비용 줄이기") lists GQA
+ * support among FlashAttention-2's additions without defining it; the plain
+ * reading taken here: q, dO, o, o32, dq are [B,H,N,d] and lse, D are [B,H,N]
+ * as above, while k, v, dk, dv are [B,Hkv,N,d], and query head h reads K / V
+ * head h / (H / Hkv) of the same batch entry (contiguous groups of H / Hkv
+ * query heads share one K / V head).  dK and dV of a K / V head are the sums
+ * over its group's query heads.  H must be a multiple of Hkv (>= 1), else
+ * ATTN_ERR_INVALID_ARG with nothing enqueued.  With Hkv = H each call is the
+ * same as the plain entry point of the same name.  dq_accum is [B,H,N,d]
+ * fp32.  Other conventions as above.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_gqa_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_train_gqa(const void* q, const void* k, const void* v, void* o, float* o32,
+                       float* lse, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                       void* stream);
+int attn_fwd_train_gqa_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                           float scale, void* stream);
+int attn_bwd_preprocess_gqa(const void* q, const void* k, const void* v, const void* dO,
+                            const float* lse, float* D, float* dq_accum, int B, int H, int Hkv,
+                            int N, int d, int causal, float scale, void* stream);
+int attn_bwd_preprocess_gqa_f16(const void* q, const void* k, const void* v, const void* dO,
+                                const float* lse, float* D, float* dq_accum, int B, int H,
+                                int Hkv, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* dO,
+                 const float* lse, const float* D, float* dq_accum,
+                 void* dq, void* dk, void* dv,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum,
+                     void* dq, void* dk, void* dv,
+                     int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+
 /* Static English description of a status code. */
 const char* attn_status_string(int status);
 

@@ -64,6 +64,16 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = at
                 fn.restype = I
+            # grouped K / V heads: one more int (Hkv) after H
+            for name, at in (("attn_fwd_gqa", fwd), ("attn_fwd_gqa_f16", fwd),
+                             ("attn_fwd_train_gqa", fwdt), ("attn_fwd_train_gqa_f16", fwdt),
+                             ("attn_bwd_preprocess_gqa", pre),
+                             ("attn_bwd_preprocess_gqa_f16", pre),
+                             ("attn_bwd_gqa", bwd), ("attn_bwd_gqa_f16", bwd)):
+                fn = getattr(L, name)
+                h = at.index(I) + 2          # position of H is the second int (B, H, ...)
+                fn.argtypes = at[:h] + [I] + at[h:]
+                fn.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -99,15 +109,23 @@ def _check(rc: int, where: str):
 # Raw C-ABI calls (pointers as ints)
 # ---------------------------------------------------------------------------
 
-def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream, f16=False):
-    fn = lib().attn_fwd_f16 if f16 else lib().attn_fwd
-    _check(fn(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale), stream),
+def _heads(name, f16, H, Hkv):
+    """The entry point for (dtype, grouping) and the head arguments it takes."""
+    grouped = Hkv is not None and Hkv != H
+    fn = getattr(lib(), name + ("_gqa" if grouped else "") + ("_f16" if f16 else ""))
+    return fn, ((H, Hkv) if grouped else (H,))
+
+
+def attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream, f16=False, Hkv=None):
+    fn, hs = _heads("attn_fwd", f16, H, Hkv)
+    _check(fn(q, k, v, o, lse, B, *hs, N, d, int(bool(causal)), float(scale), stream),
            "attn_fwd")
 
 
-def attn_fwd_train(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, f16=False):
-    fn = lib().attn_fwd_train_f16 if f16 else lib().attn_fwd_train
-    _check(fn(q, k, v, o, o32, lse, B, H, N, d, int(bool(causal)), float(scale), stream),
+def attn_fwd_train(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, f16=False,
+                   Hkv=None):
+    fn, hs = _heads("attn_fwd_train", f16, H, Hkv)
+    _check(fn(q, k, v, o, o32, lse, B, *hs, N, d, int(bool(causal)), float(scale), stream),
            "attn_fwd_train")
 
 
@@ -117,16 +135,16 @@ def attn_bwd_preprocess_o32(o32, dO, D, dq_accum, B, H, N, d, stream, f16=False)
 
 
 def attn_bwd_preprocess(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream,
-                        f16=False):
-    fn = lib().attn_bwd_preprocess_f16 if f16 else lib().attn_bwd_preprocess
-    _check(fn(q, k, v, dO, lse, D, dq_accum, B, H, N, d, int(bool(causal)), float(scale), stream),
-           "attn_bwd_preprocess")
+                        f16=False, Hkv=None):
+    fn, hs = _heads("attn_bwd_preprocess", f16, H, Hkv)
+    _check(fn(q, k, v, dO, lse, D, dq_accum, B, *hs, N, d, int(bool(causal)), float(scale),
+              stream), "attn_bwd_preprocess")
 
 
 def attn_bwd(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
-             f16=False):
-    fn = lib().attn_bwd_f16 if f16 else lib().attn_bwd
-    _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, int(bool(causal)),
+             f16=False, Hkv=None):
+    fn, hs = _heads("attn_bwd", f16, H, Hkv)
+    _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, *hs, N, d, int(bool(causal)),
               float(scale), stream), "attn_bwd")
 
 
@@ -168,26 +186,38 @@ def _check_qkv(*ts):
     return t0.shape, t0.dtype == torch.float16
 
 
+def _check_grouped(q, k, v, *qlike):
+    """Shapes for q (and dO) [B,H,N,d] with k, v [B,Hkv,N,d], H a multiple of Hkv."""
+    (B, H, N, d), f16 = _check_qkv(q, *qlike)
+    _check_qkv(k, v)
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, Nk, dk) != (B, N, d) or k.dtype != q.dtype or Hkv < 1 or H % Hkv != 0:
+        raise ValueError("k, v must be [B, Hkv, N, d] like q with H a multiple of Hkv")
+    return (B, H, Hkv, N, d), f16
+
+
 def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=None,
             o32=None):
     """O, lse for [B,H,N,d] CUDA tensors (outputs allocated by torch if not given).
 
-    With ``o32`` (an fp32 [B,H,N,d] tensor, or True to allocate one) the
-    training forward also writes O in fp32 and returns (o, lse, o32).
+    k and v may have fewer heads than q ([B,Hkv,N,d], H a multiple of Hkv):
+    groups of H / Hkv query heads then share one K / V head.  With ``o32``
+    (an fp32 [B,H,N,d] tensor, or True to allocate one) the training forward
+    also writes O in fp32 and returns (o, lse, o32).
     """
     torch = _torch()
-    (B, H, N, d), f16 = _check_qkv(q, k, v)
+    (B, H, Hkv, N, d), f16 = _check_grouped(q, k, v)
     scale = d ** -0.5 if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     if o32 is None:
         attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                 B, H, N, d, causal, scale, _stream_handle(stream), f16)
+                 B, H, N, d, causal, scale, _stream_handle(stream), f16, Hkv)
         return o, lse
     if o32 is True:
         o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
     attn_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o32.data_ptr(),
-                   lse.data_ptr(), B, H, N, d, causal, scale, _stream_handle(stream), f16)
+                   lse.data_ptr(), B, H, N, d, causal, scale, _stream_handle(stream), f16, Hkv)
     return o, lse, o32
 
 
@@ -198,9 +228,10 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
     With ``o32`` (the fp32 O of the training forward) D comes from
     rowsum(dO o O); otherwise the preprocess recomputes it from q, k, v, dO
     and lse.  ``o`` (the 16-bit forward output) is not read and may be None.
+    With grouped K / V heads, dk and dv are [B,Hkv,N,d], summed over each group.
     """
     torch = _torch()
-    (B, H, N, d), f16 = _check_qkv(q, k, v, dO)
+    (B, H, Hkv, N, d), f16 = _check_grouped(q, k, v, dO)
     scale = d ** -0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -215,10 +246,10 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
     else:
         attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(),
                             lse.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), B, H, N, d,
-                            causal, scale, s, f16)
+                            causal, scale, s, f16, Hkv)
     attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-             B, H, N, d, causal, scale, s, f16)
+             B, H, N, d, causal, scale, s, f16, Hkv)
     return dq, dk, dv
 
 

@@ -87,6 +87,9 @@ int check_shape(int B, int H, int N, int d) {
 
 int check_scale(float s) { return (std::isfinite(s) && s > 0.f) ? ATTN_OK : ATTN_ERR_INVALID_ARG; }
 
+// Grouped K / V heads: Hkv >= 1 and a divisor of H.
+int check_kv_heads(int H, int Hkv) { return (Hkv >= 1 && H % Hkv == 0) ? ATTN_OK : ATTN_ERR_INVALID_ARG; }
+
 // 3-D tensor map over a contiguous [BH, N, d] 16-bit array: box = 64 columns x
 // 128 rows x 1 head, 128-byte swizzle, zero fill beyond row N of each head.
 int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
@@ -126,20 +129,21 @@ int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
 int map_launch(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse, int B,
-             int H, int N, int d, int causal, float scale, void* stream, bool bf16) {
+             int H, int Hkv, int N, int d, int causal, float scale, void* stream, bool bf16) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (o32 != nullptr && !aligned16(o32)) return ATTN_ERR_MISALIGNED;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
+    if ((rc = check_kv_heads(H, Hkv))) return rc;
     if ((rc = check_scale(scale))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     CUtensorMap tq, tk, tv, to, to32;
-    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
-        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&to, o, BH, N, d, bf16)))
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BHkv, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BHkv, N, d, bf16)) || (rc = make_map(&to, o, BH, N, d, bf16)))
         return rc;
     // the plain forward never touches the fp32 map; it gets a copy of the O map
     if (o32 != nullptr) {
@@ -154,6 +158,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.status = status;
     a.N = N;
     a.BH = BH;
+    a.H = H;
+    a.Hkv = Hkv;
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -162,21 +168,22 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
 }
 
 int pre_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-             float* D, float* dq_accum, int B, int H, int N, int d, int causal, float scale,
-             void* stream, bool bf16) {
+             float* D, float* dq_accum, int B, int H, int Hkv, int N, int d, int causal,
+             float scale, void* stream, bool bf16) {
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
+    if ((rc = check_kv_heads(H, Hkv))) return rc;
     if ((rc = check_scale(scale))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
         !aligned16(D) || !aligned16(dq_accum))
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     CUtensorMap tq, tk, tv, tdo;
-    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
-        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BHkv, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BHkv, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
         return rc;
     DsumArgs a{};
     a.lse = lse;
@@ -185,6 +192,8 @@ int pre_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.status = status;
     a.N = N;
     a.BH = BH;
+    a.H = H;
+    a.Hkv = Hkv;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_bwd_preprocess(tq, tk, tv, tdo, a, BH, d, causal != 0, bf16,
@@ -211,12 +220,13 @@ int pre_o32_impl(const float* o32, const void* dO, float* D, float* dq_accum, in
 }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-             const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int N,
-             int d, int causal, float scale, void* stream, bool bf16) {
+             const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int Hkv,
+             int N, int d, int causal, float scale, void* stream, bool bf16) {
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
+    if ((rc = check_kv_heads(H, Hkv))) return rc;
     if ((rc = check_scale(scale))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
         !aligned16(D) || !aligned16(dq_accum) || !aligned16(dq) || !aligned16(dk) ||
@@ -224,14 +234,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     CUtensorMap tq, tk, tv, tdo;
-    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BH, N, d, bf16)) ||
-        (rc = make_map(&tv, v, BH, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
+    if ((rc = make_map(&tq, q, BH, N, d, bf16)) || (rc = make_map(&tk, k, BHkv, N, d, bf16)) ||
+        (rc = make_map(&tv, v, BHkv, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
         return rc;
     CUtensorMap tdq, tdk, tdv;
-    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d)) || (rc = make_map(&tdk, dk, BH, N, d, bf16)) ||
-        (rc = make_map(&tdv, dv, BH, N, d, bf16)))
+    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d)) || (rc = make_map(&tdk, dk, BHkv, N, d, bf16)) ||
+        (rc = make_map(&tdv, dv, BHkv, N, d, bf16)))
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     BwdArgs a{};
@@ -243,11 +253,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.status = status;
     a.N = N;
     a.BH = BH;
+    a.H = H;
+    a.Hkv = Hkv;
     a.num_kvblocks = (N + kTile - 1) / kTile;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
-    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, d, causal != 0, bf16, st))))
+    // one CTA per (batch, K / V head, key block): it loops over the head's group
+    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, BHkv, d, causal != 0, bf16, st))))
         return rc;
     DqConvertArgs c{};
     c.dq_accum = dq_accum;
@@ -281,25 +294,25 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, int causal, float scale, void* stream) {
-    return fwd_impl(q, k, v, o, nullptr, lse, B, H, N, d, causal, scale, stream, true);
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, true);
 }
 
 int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, int causal, float scale, void* stream) {
-    return fwd_impl(q, k, v, o, nullptr, lse, B, H, N, d, causal, scale, stream, false);
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, false);
 }
 
 int attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
                    int B, int H, int N, int d, int causal, float scale, void* stream) {
     if (!o32) return ATTN_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, true);
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true);
 }
 
 int attn_fwd_train_f16(const void* q, const void* k, const void* v, void* o, float* o32,
                        float* lse, int B, int H, int N, int d, int causal, float scale,
                        void* stream) {
     if (!o32) return ATTN_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, o, o32, lse, B, H, N, d, causal, scale, stream, false);
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false);
 }
 
 int attn_bwd_preprocess_o32(const float* o32, const void* dO, float* D, float* dq_accum, int B,
@@ -315,27 +328,78 @@ int attn_bwd_preprocess_o32_f16(const float* o32, const void* dO, float* D, floa
 int attn_bwd_preprocess(const void* q, const void* k, const void* v, const void* dO,
                         const float* lse, float* D, float* dq_accum, int B, int H, int N, int d,
                         int causal, float scale, void* stream) {
-    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream, true);
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, H, N, d, causal, scale, stream, true);
 }
 
 int attn_bwd_preprocess_f16(const void* q, const void* k, const void* v, const void* dO,
                             const float* lse, float* D, float* dq_accum, int B, int H, int N,
                             int d, int causal, float scale, void* stream) {
-    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, N, d, causal, scale, stream, false);
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, H, N, d, causal, scale, stream, false);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* dO, const float* lse,
              const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int N,
              int d, int causal, float scale, void* stream) {
-    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale, stream,
                     true);
 }
 
 int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                  const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H,
                  int N, int d, int causal, float scale, void* stream) {
-    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scale, stream,
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale, stream,
                     false);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, Hkv, N, d, causal, scale, stream, true);
+}
+
+int attn_fwd_gqa_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, Hkv, N, d, causal, scale, stream, false);
+}
+
+int attn_fwd_train_gqa(const void* q, const void* k, const void* v, void* o, float* o32,
+                       float* lse, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                       void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, Hkv, N, d, causal, scale, stream, true);
+}
+
+int attn_fwd_train_gqa_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                           float scale, void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, Hkv, N, d, causal, scale, stream, false);
+}
+
+int attn_bwd_preprocess_gqa(const void* q, const void* k, const void* v, const void* dO,
+                            const float* lse, float* D, float* dq_accum, int B, int H, int Hkv,
+                            int N, int d, int causal, float scale, void* stream) {
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, Hkv, N, d, causal, scale, stream, true);
+}
+
+int attn_bwd_preprocess_gqa_f16(const void* q, const void* k, const void* v, const void* dO,
+                                const float* lse, float* D, float* dq_accum, int B, int H,
+                                int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return pre_impl(q, k, v, dO, lse, D, dq_accum, B, H, Hkv, N, d, causal, scale, stream, false);
+}
+
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                 const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H,
+                 int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                    stream, true);
+}
+
+int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                     void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                     void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                    stream, false);
 }
 
 const char* attn_status_string(int s) {

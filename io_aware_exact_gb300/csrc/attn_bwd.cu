@@ -106,8 +106,9 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int lane = threadIdx.x & 31;
     const int N = args.N;
     const int nblk = (N + kTile - 1) / kTile;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x;                                      // (batch, query head)
     if (grid_block() >= nblk) return;                               // padding CTA
+    const int bkv = kv_head(bh, args.H, args.Hkv);                  // its K / V head
     const int qi = nblk - 1 - grid_block();                         // heavy query blocks first
     const int nkv = CAUSAL ? min(nblk, qi + 1) : nblk;
 
@@ -178,11 +179,11 @@ attn_bwd_dsum_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
                 for (int b = 0; b < C::KBOX; ++b)
                     tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                                bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
                 mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
                 for (int b = 0; b < C::KBOX; ++b)
                     tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                                bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
                 issued = j + 1;
             }
             if (!ok) {
@@ -428,7 +429,7 @@ __device__ __forceinline__ uint32_t dq_box_addr(uint32_t sbase, int s, int b) {
            (b % per_tile) * C::DQ_BOX_BYTES;
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool GROUPED>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -452,13 +453,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+    const int bkv = blockIdx.x;                  // (batch, K / V head)
     if (grid_block() >= args.num_kvblocks) return;                  // padding CTA
     const int j = grid_block();                  // key block (causal: small j = most work)
     const int N = args.N;
     const int nq = args.num_kvblocks;            // query blocks == key blocks
     const int i_start = CAUSAL ? j : 0;
-    const int n_it = nq - i_start;
+    const int n_i = nq - i_start;                // query blocks per query head
+    // GROUPED: the query heads of this K / V head's group, one after the other;
+    // block it of the loop is query block qblk(it) of query head qhead(it), and
+    // dK_j, dV_j accumulate over all of them.  Otherwise (Hkv = H) the one query
+    // head of the same index, without the divisions.
+    const int group = GROUPED ? args.H / args.Hkv : 1;
+    const int qh0 = GROUPED ? (bkv / args.Hkv) * args.H + (bkv % args.Hkv) * group : bkv;
+    const int n_it = group * n_i;
+    auto qhead = [&](int it) { return GROUPED ? qh0 + it / n_i : qh0; };
+    auto qblk = [&](int it) { return GROUPED ? i_start + it % n_i : i_start + it; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_KVFULL), 1);
@@ -517,14 +527,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b) {
                         tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
-                                    j * kTile, bh, pol_kv);
+                                    j * kTile, bkv, pol_kv);
                         tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
-                                    j * kTile, bh, pol_kv);
+                                    j * kTile, bkv, pol_kv);
                     }
                     // Only the first STAGES Q / dO tiles: the dQ reducer reloads each
                     // stage itself as soon as its reductions have read it (see there).
                     for (int it = 0; it < min(n_it, C::STAGES); ++it) {
-                        const int i = i_start + it;
+                        const int i = qblk(it);
+                        const int bh = qhead(it);
                         mbar_arrive_expect_tx(bar(C::B_QFULL + it), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
                             tma_load_3d(sbase + C::Q_OFF + it * C::TILE_BYTES + b * kBoxBytes, &tm_q,
@@ -628,27 +639,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         #pragma unroll
                         for (int b = 0; b < NB_Q; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
-                                              (i_start + it) * kTile, bh);
+                                              qblk(it) * kTile, qhead(it));
                         bulk_commit_group();
                         bulk_wait_group_read<0>();
                         if (nxt < n_it) {
                             mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
                             for (int b = 0; b < C::KBOX; ++b)
                                 tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                            bar(C::B_QFULL + s), b * kBoxCols, (i_start + nxt) * kTile, bh, pol_q);
+                                            bar(C::B_QFULL + s), b * kBoxCols, qblk(nxt) * kTile, qhead(nxt), pol_q);
                             issued_q = nxt + 1;
                         }
         #pragma unroll
                         for (int b = NB_Q; b < NB; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
-                                              (i_start + it) * kTile, bh);
+                                              qblk(it) * kTile, qhead(it));
                         bulk_commit_group();
                         bulk_wait_group_read<0>();
                         if (nxt < n_it) {
                             mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
                             for (int b = 0; b < C::KBOX; ++b)
                                 tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
-                                            bar(C::B_DOFULL + s), b * kBoxCols, (i_start + nxt) * kTile, bh, pol_q);
+                                            bar(C::B_DOFULL + s), b * kBoxCols, qblk(nxt) * kTile, qhead(nxt), pol_q);
                             issued_do = nxt + 1;
                         }
                     }
@@ -667,14 +678,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             } else if (warp == 3) {
                 // ------------------------------------------------------------ lse / D loader
-                const float* lse_g = args.lse + static_cast<size_t>(bh) * N;
-                const float* d_g = args.D + static_cast<size_t>(bh) * N;
                 for (int it = 0; it < n_it; ++it) {
+                    const float* lse_g = args.lse + static_cast<size_t>(qhead(it)) * N;
+                    const float* d_g = args.D + static_cast<size_t>(qhead(it)) * N;
                     const int s = it % C::STAGES;
                     if (it >= C::STAGES &&
                         !__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_STEMPTY + s), ((it / C::STAGES) - 1) & 1)))
                         break;
-                    const int q0 = (i_start + it) * kTile;
+                    const int q0 = qblk(it) * kTile;
                     float* l2 = stats + s * 2 * kTile;
                     float* dv = l2 + kTile;
         #pragma unroll
@@ -706,7 +717,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // P^T_i: wait for S^T_i and block i's statistics, write packed P^T to TMEM
                 auto compute_p = [&](int it) -> bool {
                     const int s = it % C::STAGES;
-                    const int i = i_start + it;
+                    const int i = qblk(it);
                     if (!__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL), it & 1) &&
                                                      wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1)))
                         return false;
@@ -858,7 +869,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (wq == 0 && lane == 0 && wait_bar(wc, bar(C::B_EPI + c), 0)) {
                         for (int b = 0; b < D / 64; ++b)
                             tma_store_3d(c == 0 ? &tm_dv : &tm_dk, sbase + region + b * kBoxBytes, 64 * b,
-                                         j * kTile, bh);
+                                         j * kTile, bkv);
                         bulk_commit_group();
                         bulk_wait_group_read<0>();   // shared memory read; writes complete with the kernel
                     }
@@ -906,12 +917,12 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool GROUPED>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                                 const CUtensorMap& tdv, const BwdArgs& a, int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
+    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GROUPED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -955,9 +966,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
                        bool bf16, cudaStream_t stream) {
-#define ATTN_BWD_CASE(D_, C_, B_) \
-    if (d == D_ && causal == C_ && bf16 == B_) \
-        return launch_bwd_t<D_, C_, B_>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
+    const bool grouped = a.Hkv != a.H;
+#define ATTN_BWD_CASE(D_, C_, B_)                                                              \
+    if (d == D_ && causal == C_ && bf16 == B_)                                                 \
+        return grouped ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+                       : launch_bwd_t<D_, C_, B_, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)
     ATTN_BWD_CASE(64, true, true)
     ATTN_BWD_CASE(128, false, true)

@@ -25,7 +25,9 @@ struct FwdArgs {
     float* lse;            // [B*H, N] fp32, written (natural log, scale inside)
     int* status;           // device status word
     int N;                 // sequence length
-    int BH;                // batch * heads
+    int BH;                // batch * query heads
+    int H;                 // query heads
+    int Hkv;               // key / value heads (H is a multiple; query head h reads K/V head h / (H / Hkv))
     int num_qblocks;       // ceil(N / 256): CTAs per head
     float scale_log2;      // softmax scale * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
@@ -39,7 +41,9 @@ struct BwdArgs {
     void* dv;              // [B*H, N, d] 16-bit
     int* status;
     int N;
-    int BH;                // batch * heads
+    int BH;                // batch * query heads
+    int H;                 // query heads
+    int Hkv;               // key / value heads (grid: batch * Hkv); query heads per group H / Hkv
     int num_kvblocks;      // ceil(N / 128)
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
@@ -52,7 +56,9 @@ struct DsumArgs {
     float* dq_accum;       // [B*H, N, d] fp32, zeroed
     int* status;
     int N;
-    int BH;                // batch * heads
+    int BH;                // batch * query heads
+    int H;                 // query heads
+    int Hkv;               // key / value heads
     float scale_log2;      // tau * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
@@ -115,6 +121,11 @@ inline int device_sm_count() {
         if (n <= 0) n = 152;
     }
     return n;
+}
+
+// K / V head of (batch, query head) bh when groups of H / Hkv query heads share one
+__device__ __forceinline__ int kv_head(int bh, int H, int Hkv) {
+    return (bh / H) * Hkv + (bh % H) / (H / Hkv);
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -81,8 +81,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x;                                     // (batch, query head)
     if (grid_block() >= args.num_qblocks) return;                  // padding CTA
+    const int bkv = kv_head(bh, args.H, args.Hkv);                 // its K / V head
     const int qb = args.num_qblocks - 1 - grid_block();            // heavy blocks first
     const int q0 = qb * (C::TILES * kTile);
     const int N = args.N;
@@ -158,11 +159,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                    bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                                    bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
                     mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                    bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bh, pol_kv);
+                                    bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
                     issued = j + 1;
                 }
                 if (!ok) {

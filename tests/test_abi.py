@@ -160,3 +160,17 @@ def test_library_allocates_nothing():
         for bad in (r"\bcudaMalloc", r"\bcudaFree", r"\bcuMemAlloc", r"\bmalloc\s*\(",
                     r"=\s*new\b", r"\bcudaMallocAsync"):
             assert not re.search(bad, text), (p, bad)
+
+
+def test_grouped_entry_point_argument_errors(L):
+    """H must be a positive multiple of Hkv; checked before any device call."""
+    fwd = lambda H, Hkv: L.attn_fwd_gqa(A, A, A, A, A, 1, H, Hkv, 128, 64, 1, 0.125, None)
+    assert fwd(4, 2) in (4, 0)            # valid arguments: no device here
+    assert fwd(3, 2) == 1
+    assert fwd(4, 0) == 1
+    assert fwd(2, 4) == 1
+    assert L.attn_fwd_train_gqa(A, A, A, A, A, A, 1, 4, 3, 128, 64, 1, 0.125, None) == 1
+    assert L.attn_fwd_train_gqa(A, A, A, A, None, A, 1, 4, 2, 128, 64, 1, 0.125, None) == 1
+    assert L.attn_bwd_preprocess_gqa(A, A, A, A, A, A, A, 1, 6, 4, 128, 64, 1, 0.125, None) == 1
+    assert L.attn_bwd_gqa(A, A, A, A, A, A, A, A, A, A, 1, 6, 4, 128, 64, 1, 0.125, None) == 1
+    assert L.attn_bwd_gqa(A, A, A, A, A, A, A, A, A, A, 1, 6, 3, 128, 80, 1, 0.125, None) == 2
