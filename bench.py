@@ -145,6 +145,11 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     B, H, N, d, causal = w.B, w.H, w.N, w.d, w.causal
     x = make_inputs(B, H, N, d, w.seed + 100 * rank, w.qk_mult)
+    Hkv = args.kv_heads or H
+    if H % Hkv != 0:
+        raise SystemExit("--kv-heads must divide the workload's %d heads" % H)
+    for n in ("k", "v"):          # grouped K / V heads: keep the first Hkv of each batch entry
+        x[n] = x[n][:, :Hkv].contiguous()
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
     o = torch.empty_like(q)
     o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
@@ -161,14 +166,15 @@ def run_ours(args):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        attn.attn_fwd_train(P(q), P(k), P(v), P(o), P(o32), P(lse), B, H, N, d, causal, scale, s)
+        attn.attn_fwd_train(P(q), P(k), P(v), P(o), P(o32), P(lse), B, H, N, d, causal, scale, s,
+                            Hkv=Hkv)
         if ev:
             ev[1].record(stream)
         attn.attn_bwd_preprocess_o32(P(o32), P(dO), P(D), P(acc), B, H, N, d, s)
         if ev:
             ev[2].record(stream)
         attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
-                      B, H, N, d, causal, scale, s)
+                      B, H, N, d, causal, scale, s, Hkv=Hkv)
         if ev:
             ev[3].record(stream)
 
@@ -202,13 +208,13 @@ def run_ours(args):
     # forward alone (attn_fwd: O and lse, no fp32 O), the inference forward,
     # timed per launch with the same L2 flush between launches
     for _ in range(3):
-        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s, Hkv=Hkv)
     fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
         fevs[i][0].record(stream)
-        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s)
+        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s, Hkv=Hkv)
         fevs[i][1].record(stream)
     torch.cuda.synchronize()
     if attn.attn_get_device_status() != 0:
@@ -310,7 +316,9 @@ def run_ours(args):
     bwd_tflops = flops_bwd_kernel / (ms_bwd * 1e-3) / 1e12
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
-    traffic = profile_traffic(args.workload)
+    # the committed ncu summary is of the multi-head headline workload
+    traffic = profile_traffic(args.workload) if Hkv == H else None
+    workload = args.workload if Hkv == H else "%s_gqa_kv%d" % (args.workload, Hkv)
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -325,7 +333,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), Q and K x3, bf16)",
-        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+        "config": {"workload": workload, "B": B, "H": H, "kv_heads": Hkv, "N": N, "d": d,
+                   "causal": causal,
                    "global_batch": B * world, "seq_len": N,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs 268 MB > 126 MB L2, and L2 flushed (512 MB write) between steps",
@@ -490,6 +499,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="grouped K/V heads (GQA / MQA): K and V keep only this many heads")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
