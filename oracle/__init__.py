@@ -205,3 +205,61 @@ def attention_backward_grouped(q, k, v, dO, causal: bool, scale: float):
         dk[g] += dk_h
         dv[g] += dv_h
     return dq, dk, dv, lse, D
+
+
+def _seq_bounds(cu_seqlens):
+    cu = [int(c) for c in cu_seqlens]
+    assert cu[0] == 0 and all(a <= b for a, b in zip(cu, cu[1:]))
+    return cu
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool, scale: float):
+    """Variable-length batch in the packed layout of the sj-techlog page
+    ("2. module 경계는 ..."): the valid tokens of all sequences concatenated,
+    q [total, H, d], k, v [total, Hkv, *], sequence b at tokens
+    [cu_seqlens[b], cu_seqlens[b+1]).  Each sequence attends only to itself;
+    the causal mask is per sequence.  Returns O [total, H, dv] and lse
+    [B, H, max_seqlen] (lse of the page's {batch, heads, seq_len} shape; NaN
+    past each sequence's length)."""
+    cu = _seq_bounds(cu_seqlens)
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, H, _ = q.shape
+    Hkv = k.shape[1]
+    B = len(cu) - 1
+    o = np.zeros((total, H, v.shape[2]), np.float64)
+    lse = np.full((B, H, max_seqlen), np.nan, np.float64)
+    for b in range(B):
+        s0, s1 = cu[b], cu[b + 1]
+        if s1 == s0:
+            continue
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            ob, lb = attention_forward(q[s0:s1, h], k[s0:s1, g], v[s0:s1, g], causal, scale)
+            o[s0:s1, h] = ob
+            lse[b, h, :s1 - s0] = lb
+    return o, lse
+
+
+def attention_backward_varlen(q, k, v, dO, cu_seqlens, causal: bool, scale: float):
+    """(dQ [total, H, d], dK [total, Hkv, d], dV [total, Hkv, dv]) of the
+    packed variable-length batch above: each sequence and head is the
+    single-head backward; dK, dV of a K / V head sum over its group."""
+    cu = _seq_bounds(cu_seqlens)
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    total, H, _ = q.shape
+    Hkv = k.shape[1]
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(k.shape, np.float64)
+    dv = np.zeros(v.shape, np.float64)
+    for b in range(len(cu) - 1):
+        s0, s1 = cu[b], cu[b + 1]
+        if s1 == s0:
+            continue
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            dqb, dkb, dvb, _, _ = attention_backward(q[s0:s1, h], k[s0:s1, g], v[s0:s1, g],
+                                                     dO[s0:s1, h], causal, scale)
+            dq[s0:s1, h] = dqb
+            dk[s0:s1, g] += dkb
+            dv[s0:s1, g] += dvb
+    return dq, dk, dv

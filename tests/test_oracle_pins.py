@@ -339,3 +339,59 @@ def test_grouped_backward_matches_finite_differences(H, Hkv, causal):
     for got, want in ((dq, gq), (dk, gk), (dvv, gv)):
         scale = max(1.0, np.max(np.abs(want)))
         assert np.max(np.abs(got - want)) / scale < 1e-6
+
+
+# --------------------------------------------------------------------------
+# Variable-length (packed) batches
+# --------------------------------------------------------------------------
+
+def _block_diag_attention(q, k, v, cu, causal, tau):
+    """Brute force over the concatenated tokens: score -inf between tokens of
+    different sequences (and above the diagonal within one if causal),
+    softmax over every key of the whole batch, one head at a time."""
+    total, H, _ = q.shape
+    Hkv = k.shape[1]
+    seq = np.zeros(total, np.int64)
+    for b in range(len(cu) - 1):
+        seq[cu[b]:cu[b + 1]] = b
+    pos = np.arange(total) - np.asarray(cu)[seq]
+    o = np.zeros((total, H, v.shape[2]))
+    for h in range(H):
+        g = h // (H // Hkv)
+        s = tau * q[:, h] @ k[:, g].T
+        allowed = seq[:, None] == seq[None, :]
+        if causal:
+            allowed &= pos[None, :] <= pos[:, None]
+        s = np.where(allowed, s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        o[:, h] = (p / p.sum(axis=1, keepdims=True)) @ v[:, g]
+    return o
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_forward_matches_block_diagonal_mask(causal):
+    r = _rng(60 + int(causal))
+    cu = [0, 3, 4, 4, 9]                 # lengths 3, 1, 0, 5
+    q, k, v = r.normal(size=(9, 4, 3)), r.normal(size=(9, 2, 3)), r.normal(size=(9, 2, 2))
+    o, lse = oracle.attention_forward_varlen(q, k, v, cu, 6, causal, 0.7)
+    want = _block_diag_attention(q, k, v, cu, causal, 0.7)
+    assert np.max(np.abs(o - want)) < 1e-12
+    assert np.all(np.isnan(lse[2])) and np.all(np.isnan(lse[1, :, 1:]))
+    assert np.all(np.isfinite(lse[3, :, :5]))
+
+
+def test_varlen_backward_matches_finite_differences():
+    r = _rng(70)
+    cu = [0, 2, 2, 5]
+    q, dO = r.normal(size=(5, 2, 3)), r.normal(size=(5, 2, 2))
+    k, v = r.normal(size=(5, 1, 3)), r.normal(size=(5, 1, 2))
+
+    def loss(qq, kk, vv):
+        return float(np.sum(_block_diag_attention(qq, kk, vv, cu, True, 0.7) * dO))
+
+    dq, dk, dv = oracle.attention_backward_varlen(q, k, v, dO, cu, True, 0.7)
+    for got, want in ((dq, _fd_grad(q, lambda x: loss(x, k, v))),
+                      (dk, _fd_grad(k, lambda x: loss(q, x, v))),
+                      (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
