@@ -208,6 +208,56 @@ int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO
                      void* dq, void* dk, void* dv,
                      int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/*
+ * Packed variable-length batches, following the sj-techlog page ("2. module
+ * 경계는 ..."): only the valid tokens are passed, concatenated, with
+ * cu_seqlens (the cumulative token offset of each sequence) and the maximum
+ * length, and softmax_lse is {batch, heads, seq_len}.
+ *  - q, o, dO, dq: [total, H, d]; k, v, dk, dv: [total, Hkv, d] (16-bit,
+ *    heads interleaved per token); o32, dq_accum: [total, H, d] fp32.
+ *  - cu_seqlens: device int32 [B + 1], cu_seqlens[0] = 0, non-decreasing,
+ *    cu_seqlens[B] = total; sequence b is tokens [cu_seqlens[b],
+ *    cu_seqlens[b+1]).  Empty sequences are allowed.  Each sequence attends
+ *    only to itself; the causal mask is per sequence (key j of a sequence is
+ *    visible to its query i iff j <= i).  Grouped K / V heads as above.
+ *  - lse: [B, H, max_seqlen] fp32, entries past a sequence's length are not
+ *    written.  D: [total, H] fp32 (one value per packed row).
+ *  - max_seqlen must be >= every length (the kernels clamp offsets to
+ *    [0, total] and lengths to max_seqlen, so a bad cu_seqlens gives wrong
+ *    results but no access outside the arrays); total = 0 enqueues nothing.
+ *  - The training path is attn_fwd_train_varlen, then
+ *    attn_bwd_preprocess_o32_varlen (D from the fp32 O), then attn_bwd_varlen.
+ * Argument errors (null pointers, B < 1, total < 0, max_seqlen outside
+ * 1..2^24, H not a multiple of Hkv, cu_seqlens not 4-byte aligned) return
+ * ATTN_ERR_INVALID_ARG with nothing enqueued.  Other conventions as above.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                    int d, int causal, float scale, void* stream);
+int attn_fwd_varlen_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                        int d, int causal, float scale, void* stream);
+int attn_fwd_train_varlen(const void* q, const void* k, const void* v, void* o, float* o32,
+                          float* lse, const int* cu_seqlens, int B, int total, int max_seqlen,
+                          int H, int Hkv, int d, int causal, float scale, void* stream);
+int attn_fwd_train_varlen_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                              float* lse, const int* cu_seqlens, int B, int total, int max_seqlen,
+                              int H, int Hkv, int d, int causal, float scale, void* stream);
+int attn_bwd_preprocess_o32_varlen(const float* o32, const void* dO, float* D, float* dq_accum,
+                                   int total, int H, int d, void* stream);
+int attn_bwd_preprocess_o32_varlen_f16(const float* o32, const void* dO, float* D,
+                                       float* dq_accum, int total, int H, int d, void* stream);
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* dO,
+                    const float* lse, const float* D, float* dq_accum,
+                    void* dq, void* dk, void* dv, const int* cu_seqlens,
+                    int B, int total, int max_seqlen, int H, int Hkv, int d, int causal,
+                    float scale, void* stream);
+int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void* dO,
+                        const float* lse, const float* D, float* dq_accum,
+                        void* dq, void* dk, void* dv, const int* cu_seqlens,
+                        int B, int total, int max_seqlen, int H, int Hkv, int d, int causal,
+                        float scale, void* stream);
+
 /* Static English description of a status code. */
 const char* attn_status_string(int status);
 

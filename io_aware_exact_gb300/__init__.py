@@ -74,6 +74,19 @@ def lib():
                 h = at.index(I) + 2          # position of H is the second int (B, H, ...)
                 fn.argtypes = at[:h] + [I] + at[h:]
                 fn.restype = I
+            # packed variable-length batches
+            vfwd = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+            vfwdt = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+            vpre = [P, P, P, P, I, I, I, P]
+            vbwd = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+            for name, at in (("attn_fwd_varlen", vfwd), ("attn_fwd_varlen_f16", vfwd),
+                             ("attn_fwd_train_varlen", vfwdt), ("attn_fwd_train_varlen_f16", vfwdt),
+                             ("attn_bwd_preprocess_o32_varlen", vpre),
+                             ("attn_bwd_preprocess_o32_varlen_f16", vpre),
+                             ("attn_bwd_varlen", vbwd), ("attn_bwd_varlen_f16", vbwd)):
+                fn = getattr(L, name)
+                fn.argtypes = at
+                fn.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -292,3 +305,80 @@ def attention(q, k, v, causal: bool = False, scale=None):
 
 
 AttnFunction = None
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length batches
+# ---------------------------------------------------------------------------
+
+def _check_varlen(q, k, v, cu_seqlens, *qlike):
+    torch = _torch()
+    for t in (q, k, v) + qlike:
+        if t.dim() != 3 or not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("expected contiguous CUDA [total, heads, d] tensors of one dtype")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("expected bfloat16 or float16 tensors")
+    total, H, d = q.shape
+    if k.shape != v.shape or k.shape[0] != total or k.shape[2] != d:
+        raise ValueError("k, v must be [total, Hkv, d] like q")
+    for t in qlike:
+        if t.shape != q.shape:
+            raise ValueError("dO must be shaped like q")
+    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda
+            or cu_seqlens.numel() < 2):
+        raise ValueError("cu_seqlens must be a CUDA int32 vector of B + 1 offsets")
+    return (cu_seqlens.numel() - 1, total, H, k.shape[1], d), q.dtype == torch.float16
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale=None,
+                   o=None, lse=None, o32=None, stream=None):
+    """O [total, H, d] and lse [B, H, max_seqlen] of a packed variable-length
+    batch (sequence b is tokens cu_seqlens[b]:cu_seqlens[b+1] of q, k, v).
+    With ``o32`` (True or an fp32 [total, H, d] tensor) the training forward
+    also writes O in fp32 and returns (o, lse, o32)."""
+    torch = _torch()
+    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens)
+    scale = d ** -0.5 if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, max_seqlen), dtype=torch.float32, device=q.device)
+    s = _stream_handle(stream)
+    args = (cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d, int(bool(causal)), scale, s)
+    L = lib()
+    if o32 is None:
+        fn = L.attn_fwd_varlen_f16 if f16 else L.attn_fwd_varlen
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), *args),
+               "attn_fwd_varlen")
+        return o, lse
+    if o32 is True:
+        o32 = torch.empty((total, H, d), dtype=torch.float32, device=q.device)
+    fn = L.attn_fwd_train_varlen_f16 if f16 else L.attn_fwd_train_varlen
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o32.data_ptr(),
+              lse.data_ptr(), *args), "attn_fwd_train_varlen")
+    return o, lse, o32
+
+
+def backward_varlen(q, k, v, o32, lse, dO, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale=None, dq=None, dk=None, dv=None, D=None, dq_accum=None, stream=None):
+    """dQ, dK, dV of a packed variable-length batch, from the training
+    forward's fp32 O and lse (D = rowsum(dO o O))."""
+    torch = _torch()
+    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens, dO)
+    scale = d ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    D = torch.empty((total, H), dtype=torch.float32, device=q.device) if D is None else D
+    if dq_accum is None:
+        dq_accum = torch.empty((total, H, d), dtype=torch.float32, device=q.device)
+    s = _stream_handle(stream)
+    L = lib()
+    pre = L.attn_bwd_preprocess_o32_varlen_f16 if f16 else L.attn_bwd_preprocess_o32_varlen
+    _check(pre(o32.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), total, H, d, s),
+           "attn_bwd_preprocess_o32_varlen")
+    fn = L.attn_bwd_varlen_f16 if f16 else L.attn_bwd_varlen
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+              cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d, int(bool(causal)),
+              scale, s), "attn_bwd_varlen")
+    return dq, dk, dv

@@ -270,6 +270,163 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     return map_launch(launch_dq_convert(c, bf16, st));
 }
 
+// Tensor maps over a packed variable-length [total, Hh, d] array (the valid
+// tokens of all sequences concatenated, heads interleaved): dimensions
+// (d, token, head) with strides (Hh * d, d) elements, so the kernels address it
+// with the same (column, row, head) coordinates as a dense [BH, N, d] array.
+int make_map_packed(CUtensorMap* m, const void* base, int total, int Hh, int d, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return ATTN_ERR_LAUNCH;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(total),
+                                static_cast<cuuint64_t>(Hh)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hh) * d * 2, static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kTile), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int make_map_packed_f32(CUtensorMap* m, const void* base, int total, int Hh, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return ATTN_ERR_LAUNCH;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(total),
+                                static_cast<cuuint64_t>(Hh)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hh) * d * 4, static_cast<cuuint64_t>(d) * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTile), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int check_varlen(const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d) {
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || total < 0 || max_seqlen < 1 || max_seqlen > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    if (H < 1 || static_cast<long long>(total) * H > 2147483647LL) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H > 2147483647LL) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+    return check_kv_heads(H, Hkv);
+}
+
+int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
+                    const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d,
+                    int causal, float scale, void* stream, bool bf16) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    int rc = check_varlen(cu_seqlens, B, total, max_seqlen, H, Hkv, d);
+    if (rc) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (o32 != nullptr && !aligned16(o32)))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    if (total == 0) return ATTN_OK;   // no tokens: nothing to compute
+    CUtensorMap tq, tk, tv, to, to32;
+    if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&tk, k, total, Hkv, d, bf16)) ||
+        (rc = make_map_packed(&tv, v, total, Hkv, d, bf16)) || (rc = make_map_packed(&to, o, total, H, d, bf16)))
+        return rc;
+    if (o32 != nullptr) {
+        if ((rc = make_map_packed_f32(&to32, o32, total, H, d))) return rc;
+    } else {
+        to32 = to;
+    }
+    FwdArgs a{};
+    a.o = o;
+    a.o32 = o32;
+    a.lse = lse;
+    a.status = status;
+    a.N = max_seqlen;
+    a.BH = B * H;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.num_qblocks = (max_seqlen + 2 * kTile - 1) / (2 * kTile);
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    a.max_seqlen = max_seqlen;
+    a.scale_log2 = scale * kLog2e;
+    a.wait_polls = kDefaultWaitPolls;
+    return map_launch(launch_fwd(tq, tk, tv, to, to32, a, B * H, d, causal != 0, bf16,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int pre_o32_varlen_impl(const float* o32, const void* dO, float* D, float* dq_accum, int total,
+                        int H, int d, void* stream, bool bf16) {
+    if (!o32 || !dO || !D || !dq_accum) return ATTN_ERR_INVALID_ARG;
+    if (total < 0 || H < 1 || static_cast<long long>(total) * H > 2147483647LL) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!aligned16(o32) || !aligned16(dO) || !aligned16(D) || !aligned16(dq_accum))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    int rc = current_device(&status);
+    if (rc) return rc;
+    if (total == 0) return ATTN_OK;
+    // the packed [total, H, d] rows, one D value per row: D is [total, H]
+    PreO32Args a{};
+    a.o32 = o32;
+    a.dO = dO;
+    a.D = D;
+    a.dq_accum = dq_accum;
+    a.rows = static_cast<long long>(total) * H;
+    a.d = d;
+    return map_launch(launch_bwd_preprocess_o32(a, bf16, static_cast<cudaStream_t>(stream)));
+}
+
+int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                    const float* D, float* dq_accum, void* dq, void* dk, void* dv,
+                    const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d,
+                    int causal, float scale, void* stream, bool bf16) {
+    if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
+        return ATTN_ERR_INVALID_ARG;
+    int rc = check_varlen(cu_seqlens, B, total, max_seqlen, H, Hkv, d);
+    if (rc) return rc;
+    if ((rc = check_scale(scale))) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+        !aligned16(D) || !aligned16(dq_accum) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    if ((rc = current_device(&status))) return rc;
+    if (total == 0) return ATTN_OK;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+    if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&tk, k, total, Hkv, d, bf16)) ||
+        (rc = make_map_packed(&tv, v, total, Hkv, d, bf16)) || (rc = make_map_packed(&tdo, dO, total, H, d, bf16)) ||
+        (rc = make_map_packed_f32(&tdq, dq_accum, total, H, d)) ||
+        (rc = make_map_packed(&tdk, dk, total, Hkv, d, bf16)) || (rc = make_map_packed(&tdv, dv, total, Hkv, d, bf16)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BwdArgs a{};
+    a.lse = lse;
+    a.D = D;
+    a.dq_accum = dq_accum;
+    a.dk = dk;
+    a.dv = dv;
+    a.status = status;
+    a.N = max_seqlen;
+    a.BH = B * H;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.num_kvblocks = (max_seqlen + kTile - 1) / kTile;
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    a.max_seqlen = max_seqlen;
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.wait_polls = kDefaultWaitPolls;
+    // one CTA per (sequence, K / V head, key block); blocks past a sequence exit
+    if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, B * Hkv, d, causal != 0, bf16, st))))
+        return rc;
+    DqConvertArgs c{};
+    c.dq_accum = dq_accum;
+    c.dq = dq;
+    c.elems = static_cast<long long>(total) * H * d;
+    c.scale = scale;
+    return map_launch(launch_dq_convert(c, bf16, st));
+}
+
 __global__ void selftest_timeout_kernel(int* status, unsigned int max_polls) {
     __shared__ __align__(8) uint64_t bar_storage;
     __shared__ int abort_flag;
@@ -400,6 +557,62 @@ int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO
                      void* stream) {
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
                     stream, false);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                    int d, int causal, float scale, void* stream) {
+    return fwd_varlen_impl(q, k, v, o, nullptr, lse, cu_seqlens, B, total, max_seqlen, H, Hkv, d,
+                           causal, scale, stream, true);
+}
+
+int attn_fwd_varlen_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                        int d, int causal, float scale, void* stream) {
+    return fwd_varlen_impl(q, k, v, o, nullptr, lse, cu_seqlens, B, total, max_seqlen, H, Hkv, d,
+                           causal, scale, stream, false);
+}
+
+int attn_fwd_train_varlen(const void* q, const void* k, const void* v, void* o, float* o32,
+                          float* lse, const int* cu_seqlens, int B, int total, int max_seqlen,
+                          int H, int Hkv, int d, int causal, float scale, void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, o32, lse, cu_seqlens, B, total, max_seqlen, H, Hkv, d,
+                           causal, scale, stream, true);
+}
+
+int attn_fwd_train_varlen_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                              float* lse, const int* cu_seqlens, int B, int total, int max_seqlen,
+                              int H, int Hkv, int d, int causal, float scale, void* stream) {
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, o32, lse, cu_seqlens, B, total, max_seqlen, H, Hkv, d,
+                           causal, scale, stream, false);
+}
+
+int attn_bwd_preprocess_o32_varlen(const float* o32, const void* dO, float* D, float* dq_accum,
+                                   int total, int H, int d, void* stream) {
+    return pre_o32_varlen_impl(o32, dO, D, dq_accum, total, H, d, stream, true);
+}
+
+int attn_bwd_preprocess_o32_varlen_f16(const float* o32, const void* dO, float* D,
+                                       float* dq_accum, int total, int H, int d, void* stream) {
+    return pre_o32_varlen_impl(o32, dO, D, dq_accum, total, H, d, stream, false);
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                    const float* D, float* dq_accum, void* dq, void* dk, void* dv,
+                    const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d,
+                    int causal, float scale, void* stream) {
+    return bwd_varlen_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, cu_seqlens, B, total,
+                           max_seqlen, H, Hkv, d, causal, scale, stream, true);
+}
+
+int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void* dO,
+                        const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                        void* dv, const int* cu_seqlens, int B, int total, int max_seqlen, int H,
+                        int Hkv, int d, int causal, float scale, void* stream) {
+    return bwd_varlen_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, cu_seqlens, B, total,
+                           max_seqlen, H, Hkv, d, causal, scale, stream, false);
 }
 
 const char* attn_status_string(int s) {

@@ -429,7 +429,7 @@ __device__ __forceinline__ uint32_t dq_box_addr(uint32_t sbase, int s, int b) {
            (b % per_tile) * C::DQ_BOX_BYTES;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GROUPED>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -456,19 +456,38 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int bkv = blockIdx.x;                  // (batch, K / V head)
     if (grid_block() >= args.num_kvblocks) return;                  // padding CTA
     const int j = grid_block();                  // key block (causal: small j = most work)
-    const int N = args.N;
-    const int nq = args.num_kvblocks;            // query blocks == key blocks
+    // GENERAL (grouped K / V heads and / or a packed variable-length batch): the
+    // query heads of this K / V head's group, one after the other; block it of
+    // the loop is query block qblk(it) of query head qhead(it), and dK_j, dV_j
+    // accumulate over all of them.  Rows of the sequence start at token tok0.
+    // Otherwise (dense, Hkv = H) the one query head of the same index, without
+    // the divisions.  TMA head coordinates: kvc for K, V, dK, dV and qhead(it)
+    // for Q, dO, dQ; qflat(it) is the (batch, head) index of the lse / D rows.
+    int N = args.N, tok0 = 0, kvc = bkv, qc0 = bkv, qf0 = bkv, group = 1;
+    bool varlen = false;
+    if constexpr (GENERAL) {
+        const int b = bkv / args.Hkv, kvh = bkv % args.Hkv;
+        group = args.H / args.Hkv;
+        qf0 = b * args.H + kvh * group;
+        qc0 = qf0;
+        if (args.cu_seqlens != nullptr) {
+            varlen = true;
+            const int s0 = min(max(args.cu_seqlens[b], 0), args.total);
+            const int s1 = min(max(args.cu_seqlens[b + 1], s0), args.total);
+            tok0 = s0;
+            N = min(s1 - s0, args.max_seqlen);
+            kvc = kvh;
+            qc0 = kvh * group;
+            if (j * kTile >= N) return;                             // past this sequence
+        }
+    }
+    const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks == key blocks
     const int i_start = CAUSAL ? j : 0;
     const int n_i = nq - i_start;                // query blocks per query head
-    // GROUPED: the query heads of this K / V head's group, one after the other;
-    // block it of the loop is query block qblk(it) of query head qhead(it), and
-    // dK_j, dV_j accumulate over all of them.  Otherwise (Hkv = H) the one query
-    // head of the same index, without the divisions.
-    const int group = GROUPED ? args.H / args.Hkv : 1;
-    const int qh0 = GROUPED ? (bkv / args.Hkv) * args.H + (bkv % args.Hkv) * group : bkv;
     const int n_it = group * n_i;
-    auto qhead = [&](int it) { return GROUPED ? qh0 + it / n_i : qh0; };
-    auto qblk = [&](int it) { return GROUPED ? i_start + it % n_i : i_start + it; };
+    auto qhead = [&](int it) { return GENERAL ? qc0 + it / n_i : qc0; };
+    auto qflat = [&](int it) { return GENERAL ? qf0 + it / n_i : qf0; };
+    auto qblk = [&](int it) { return GENERAL ? i_start + it % n_i : i_start + it; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_KVFULL), 1);
@@ -527,9 +546,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b) {
                         tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
-                                    j * kTile, bkv, pol_kv);
+                                    tok0 + j * kTile, kvc, pol_kv);
                         tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
-                                    j * kTile, bkv, pol_kv);
+                                    tok0 + j * kTile, kvc, pol_kv);
                     }
                     // Only the first STAGES Q / dO tiles: the dQ reducer reloads each
                     // stage itself as soon as its reductions have read it (see there).
@@ -539,11 +558,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         mbar_arrive_expect_tx(bar(C::B_QFULL + it), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
                             tma_load_3d(sbase + C::Q_OFF + it * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                        bar(C::B_QFULL + it), b * kBoxCols, i * kTile, bh, pol_q);
+                                        bar(C::B_QFULL + it), b * kBoxCols, tok0 + i * kTile, bh, pol_q);
                         mbar_arrive_expect_tx(bar(C::B_DOFULL + it), C::TILE_BYTES);
                         for (int b = 0; b < C::KBOX; ++b)
                             tma_load_3d(sbase + C::DO_OFF + it * C::TILE_BYTES + b * kBoxBytes, &tm_do,
-                                        bar(C::B_DOFULL + it), b * kBoxCols, i * kTile, bh, pol_q);
+                                        bar(C::B_DOFULL + it), b * kBoxCols, tok0 + i * kTile, bh, pol_q);
                     }
                 }
             } else if (warp == 1) {
@@ -639,27 +658,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         #pragma unroll
                         for (int b = 0; b < NB_Q; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
-                                              qblk(it) * kTile, qhead(it));
+                                              tok0 + qblk(it) * kTile, qhead(it));
                         bulk_commit_group();
                         bulk_wait_group_read<0>();
                         if (nxt < n_it) {
                             mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
                             for (int b = 0; b < C::KBOX; ++b)
                                 tma_load_3d(sbase + C::Q_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                            bar(C::B_QFULL + s), b * kBoxCols, qblk(nxt) * kTile, qhead(nxt), pol_q);
+                                            bar(C::B_QFULL + s), b * kBoxCols, tok0 + qblk(nxt) * kTile, qhead(nxt), pol_q);
                             issued_q = nxt + 1;
                         }
         #pragma unroll
                         for (int b = NB_Q; b < NB; ++b)
                             tma_reduce_add_3d(&tm_dq, dq_box_addr<D>(sbase, s, b), b * C::DQ_BOX_COLS,
-                                              qblk(it) * kTile, qhead(it));
+                                              tok0 + qblk(it) * kTile, qhead(it));
                         bulk_commit_group();
                         bulk_wait_group_read<0>();
                         if (nxt < n_it) {
                             mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
                             for (int b = 0; b < C::KBOX; ++b)
                                 tma_load_3d(sbase + C::DO_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_do,
-                                            bar(C::B_DOFULL + s), b * kBoxCols, qblk(nxt) * kTile, qhead(nxt), pol_q);
+                                            bar(C::B_DOFULL + s), b * kBoxCols, tok0 + qblk(nxt) * kTile, qhead(nxt), pol_q);
                             issued_do = nxt + 1;
                         }
                     }
@@ -679,8 +698,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             } else if (warp == 3) {
                 // ------------------------------------------------------------ lse / D loader
                 for (int it = 0; it < n_it; ++it) {
-                    const float* lse_g = args.lse + static_cast<size_t>(qhead(it)) * N;
-                    const float* d_g = args.D + static_cast<size_t>(qhead(it)) * N;
+                    // lse is [B*H, N] (varlen: [B*H, max_seqlen]); D is [B*H, N]
+                    // (varlen: [total, H], one stride of H between the rows of a head)
+                    const float* lse_g = args.lse + static_cast<size_t>(qflat(it)) *
+                                                        (varlen ? args.max_seqlen : N);
+                    const float* d_g = varlen ? args.D + static_cast<size_t>(tok0) * args.H + qflat(it) % args.H
+                                              : args.D + static_cast<size_t>(qflat(it)) * N;
+                    const size_t dstr = varlen ? static_cast<size_t>(args.H) : 1;
                     const int s = it % C::STAGES;
                     if (it >= C::STAGES &&
                         !__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_STEMPTY + s), ((it / C::STAGES) - 1) & 1)))
@@ -694,7 +718,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const bool valid = qi < N;
                         // P = exp(tau s - lse) = exp2(tau log2e s - lse log2e); rows past N get P = 0
                         l2[lane * 4 + e] = valid ? -lse_g[qi] * kLog2e : -INFINITY;
-                        dv[lane * 4 + e] = valid ? -d_g[qi] : 0.f;
+                        dv[lane * 4 + e] = valid ? -d_g[qi * dstr] : 0.f;
                     }
                     mbar_arrive(bar(C::B_STFULL + s));
                 }
@@ -848,6 +872,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
                     const int region = (c == 0) ? C::V_OFF : C::K_OFF;
                     uint8_t* stage_row = smem + region + r * 128;
+                    // The last, partial key block of a packed sequence: a TMA box would
+                    // also cover the first rows of the next sequence, so each thread
+                    // stores its own key row (rows past the sequence are not written).
+                    const bool direct = varlen && (j + 1) * kTile > N;
+                    uint16_t* drow = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
+                                     (static_cast<size_t>(tok0 + j * kTile + r) * args.Hkv + kvc) * D;
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
@@ -857,6 +887,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 16; ++e)
                             pk[e] = pack2<BF16>(__uint_as_float(a32[2 * e]) * mul,
                                                 __uint_as_float(a32[2 * e + 1]) * mul);
+                        if (direct) {
+                            if (key_ok) {
+        #pragma unroll
+                                for (int v4 = 0; v4 < 4; ++v4)
+                                    *reinterpret_cast<uint4*>(drow + cc + 8 * v4) =
+                                        make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                            }
+                            continue;
+                        }
                         uint8_t* box_row = stage_row + (cc / 64) * kBoxBytes;
                         const int ch0 = (cc % 64) / 8;
         #pragma unroll
@@ -864,12 +903,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
                                 make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(C::B_EPI + c));
-                    if (wq == 0 && lane == 0 && wait_bar(wc, bar(C::B_EPI + c), 0)) {
+                    if (direct) ok = false;   // stored; skip the TMA store below
+                    if (ok) {
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(C::B_EPI + c));
+                    }
+                    if (ok && wq == 0 && lane == 0 && wait_bar(wc, bar(C::B_EPI + c), 0)) {
                         for (int b = 0; b < D / 64; ++b)
                             tma_store_3d(c == 0 ? &tm_dv : &tm_dk, sbase + region + b * kBoxBytes, 64 * b,
-                                         j * kTile, bkv);
+                                         tok0 + j * kTile, kvc);
                         bulk_commit_group();
                         bulk_wait_group_read<0>();   // shared memory read; writes complete with the kernel
                     }
@@ -917,12 +959,12 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GROUPED>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                                 const CUtensorMap& tdv, const BwdArgs& a, int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GROUPED>;
+    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GENERAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -966,10 +1008,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
                        bool bf16, cudaStream_t stream) {
-    const bool grouped = a.Hkv != a.H;
+    const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr;
 #define ATTN_BWD_CASE(D_, C_, B_)                                                              \
     if (d == D_ && causal == C_ && bf16 == B_)                                                 \
-        return grouped ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+        return general ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
                        : launch_bwd_t<D_, C_, B_, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)
     ATTN_BWD_CASE(64, true, true)

@@ -29,6 +29,12 @@ struct FwdArgs {
     int H;                 // query heads
     int Hkv;               // key / value heads (H is a multiple; query head h reads K/V head h / (H / Hkv))
     int num_qblocks;       // ceil(N / 256): CTAs per head
+    // Packed variable-length batch (nullptr: dense [B,H,N,d]): sequence b is
+    // tokens [cu_seqlens[b], cu_seqlens[b+1]) of [total, H, d]; N = max_seqlen
+    // then, and lse is [B, H, max_seqlen].
+    const int* cu_seqlens;
+    int total;
+    int max_seqlen;
     float scale_log2;      // softmax scale * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
@@ -45,6 +51,11 @@ struct BwdArgs {
     int H;                 // query heads
     int Hkv;               // key / value heads (grid: batch * Hkv); query heads per group H / Hkv
     int num_kvblocks;      // ceil(N / 128)
+    // packed variable-length batch as in FwdArgs (nullptr: dense); D is then
+    // [total, H] (the row order of the packed tensors), lse [B, H, max_seqlen]
+    const int* cu_seqlens;
+    int total;
+    int max_seqlen;
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)

@@ -65,7 +65,7 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -83,10 +83,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x;                                     // (batch, query head)
     if (grid_block() >= args.num_qblocks) return;                  // padding CTA
-    const int bkv = kv_head(bh, args.H, args.Hkv);                 // its K / V head
     const int qb = args.num_qblocks - 1 - grid_block();            // heavy blocks first
     const int q0 = qb * (C::TILES * kTile);
-    const int N = args.N;
+    // TMA coordinates: the rows of this sequence start at tok0, the head
+    // coordinate is hq for Q / O and hk for K / V.  Dense [B,H,N,d]: tok0 = 0
+    // and the head coordinate is the (batch, head) index.  Packed variable
+    // length [total, H, d]: tok0 is the sequence's first token, N its length.
+    int tok0 = 0, N = args.N, hq = bh;
+    int hk = kv_head(bh, args.H, args.Hkv);                        // its K / V head
+    if constexpr (VARLEN) {
+        const int b = bh / args.H, h = bh % args.H;
+        const int s0 = min(max(args.cu_seqlens[b], 0), args.total);
+        const int s1 = min(max(args.cu_seqlens[b + 1], s0), args.total);
+        tok0 = s0;
+        N = min(s1 - s0, args.max_seqlen);
+        hq = h;
+        hk = h / (args.H / args.Hkv);
+        if (q0 >= N) return;                                       // past this sequence
+    }
     const int nkv_all = (N + kTile - 1) / kTile;
     int nkv[2];
 #pragma unroll
@@ -147,7 +161,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int t = 0; t < ntiles; ++t)
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::Q_OFF + t * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                    bar(C::B_QFULL), b * kBoxCols, q0 + kTile * t, bh, pol_q);
+                                    bar(C::B_QFULL), b * kBoxCols, tok0 + q0 + kTile * t, hq, pol_q);
                 int issued = 0;
                 bool ok = true;
                 for (int j = 0; j < n_iter; ++j) {
@@ -159,11 +173,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                    bar(C::B_KFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
+                                    bar(C::B_KFULL + s), b * kBoxCols, tok0 + j * kTile, hk, pol_kv);
                     mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                    bar(C::B_VFULL + s), b * kBoxCols, j * kTile, bkv, pol_kv);
+                                    bar(C::B_VFULL + s), b * kBoxCols, tok0 + j * kTile, hk, pol_kv);
                     issued = j + 1;
                 }
                 if (!ok) {
@@ -357,7 +371,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint8_t* stage_row = smem + C::Q_OFF + t * C::TILE_BYTES + r * 128;
                 const int row0 = q0 + kTile * t;
                 constexpr int ROUNDS = TRAIN ? 3 : 1;
-                for (int k = 0; k < ROUNDS && ok; ++k) {
+                if (VARLEN && row0 + kTile > N) {
+                    // The last, partial tile of a sequence: a TMA box would also cover
+                    // the first rows of the next sequence, so each thread stores its
+                    // own row (rows past the sequence are not written).
+                    const size_t rbase = (static_cast<size_t>(tok0 + row) * args.H + hq) * D;
+    #pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t orr[32];
+                        tmem_ld_sync(o_addr + c, orr);
+                        if (row < N) {
+                            if constexpr (TRAIN) {
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    *reinterpret_cast<float4*>(args.o32 + rbase + c + 4 * e) =
+                                        make_float4(__uint_as_float(orr[4 * e]) * inv_l,
+                                                    __uint_as_float(orr[4 * e + 1]) * inv_l,
+                                                    __uint_as_float(orr[4 * e + 2]) * inv_l,
+                                                    __uint_as_float(orr[4 * e + 3]) * inv_l);
+                            }
+                            uint32_t pk[16];
+    #pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                                    __uint_as_float(orr[2 * e + 1]) * inv_l);
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + rbase + c + 8 * e) =
+                                    make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
+                    }
+                }
+                for (int k = 0; k < ROUNDS && ok && !(VARLEN && row0 + kTile > N); ++k) {
                     const bool f32 = TRAIN && k < 2;
                     if (k > 0) {
                         ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_EPI_FREE + t), (k - 1) & 1));
@@ -403,10 +448,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (wait_bar(wc, bar(C::B_EPI_STAGED + t), k & 1)) {
                             if (f32) {
                                 for (int b = 0; b < D / 64; ++b)
-                                    tma_store_3d(&tm_o32, stage + b * kBoxBytes, k * (D / 2) + 32 * b, row0, bh);
+                                    tma_store_3d(&tm_o32, stage + b * kBoxBytes, k * (D / 2) + 32 * b, tok0 + row0, hq);
                             } else {
                                 for (int b = 0; b < D / 64; ++b)
-                                    tma_store_3d(&tm_o, stage + b * kBoxBytes, 64 * b, row0, bh);
+                                    tma_store_3d(&tm_o, stage + b * kBoxBytes, 64 * b, tok0 + row0, hq);
                             }
                             bulk_commit_group();
                             bulk_wait_group_read<0>();
@@ -418,7 +463,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // CTA exits (done above); their global writes complete with the
                 // kernel, and waiting for them here kept the next CTA off the SM.
                 if (row < N)
-                    args.lse[static_cast<size_t>(bh) * N + row] = (m_ref + __log2f(l)) * kLn2;
+                    args.lse[static_cast<size_t>(bh) * (VARLEN ? args.max_seqlen : N) + row] =
+                        (m_ref + __log2f(l)) * kLn2;
             }
         }
     }
@@ -431,13 +477,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to,
                                 const CUtensorMap& to32, const FwdArgs& a, int BH,
                                 cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN>;
+    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -449,10 +495,15 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
                        int d, bool causal, bool bf16, cudaStream_t stream) {
-#define ATTN_FWD_CASE(D_, C_, B_) \
-    if (d == D_ && causal == C_ && bf16 == B_)                                  \
-        return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true>(tq, tk, tv, to, to32, a, BH, stream) \
-                                : launch_fwd_t<D_, C_, B_, false>(tq, tk, tv, to, to32, a, BH, stream);
+    const bool varlen = a.cu_seqlens != nullptr;
+#define ATTN_FWD_CASE(D_, C_, B_)                                                                   \
+    if (d == D_ && causal == C_ && bf16 == B_) {                                                    \
+        if (varlen)                                                                                 \
+            return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true, true>(tq, tk, tv, to, to32, a, BH, stream) \
+                                    : launch_fwd_t<D_, C_, B_, false, true>(tq, tk, tv, to, to32, a, BH, stream); \
+        return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true, false>(tq, tk, tv, to, to32, a, BH, stream) \
+                                : launch_fwd_t<D_, C_, B_, false, false>(tq, tk, tv, to, to32, a, BH, stream); \
+    }
     ATTN_FWD_CASE(64, false, true)
     ATTN_FWD_CASE(64, true, true)
     ATTN_FWD_CASE(128, false, true)
