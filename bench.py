@@ -439,6 +439,78 @@ def _ref_sample(w, x, rows, cols, lse_all, D_all):
     return time.perf_counter() - t0
 
 
+def run_varlen(args):
+    """The training step (forward with fp32 O, D preprocess, backward) on a
+    packed variable-length batch: 32 sequences, lengths drawn uniformly from
+    [256, 8192] (seeded), H = 16, d = 128, causal, Q and K x3.  FLOPs count
+    only the real tokens: sum over sequences of 10 H L^2 d / 2, no padding."""
+    import torch
+    import numpy as np
+    import io_aware_exact_gb300 as attn
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(1234)
+    lengths = rng.integers(256, 8193, size=32)
+    H, d = 16, 128
+    Hkv = args.kv_heads or H
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    total, max_s = int(cu[-1]), int(lengths.max())
+    g = torch.Generator(device="cpu")
+    g.manual_seed(4321)
+    mk = lambda h, m: (torch.randn((total, h, d), generator=g) * m).to(torch.bfloat16).to(dev)
+    q, k, v, dO = mk(H, 3.0), mk(Hkv, 3.0), mk(Hkv, 1.0), mk(H, 1.0)
+    cu_d = torch.from_numpy(cu).to(dev)
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    o32 = torch.empty((total, H, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((len(lengths), H, max_s), dtype=torch.float32, device=dev)
+    D = torch.empty((total, H), dtype=torch.float32, device=dev)
+    acc = torch.empty((total, H, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(mid=None):
+        attn.forward_varlen(q, k, v, cu_d, max_s, True, scale, o=o, lse=lse, o32=o32, stream=stream)
+        if mid is not None:
+            mid.record(stream)
+        attn.backward_varlen(q, k, v, o32, lse, dO, cu_d, max_s, True, scale, dq=dq, dk=dk, dv=dv,
+                             D=D, dq_accum=acc, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step(evs[i][2])
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during the varlen steps")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_fwd = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    flops = float(sum(10.0 * H * int(L) * int(L) * d / 2 for L in lengths))
+    padded = 10.0 * H * len(lengths) * max_s * max_s * d / 2
+    peak = _peaks().get("bf16_tflops_sustained")
+    print(json.dumps({
+        "metric": "attention TFLOPS fwd+bwd, packed variable-length batch (real tokens only)",
+        "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1), Q and K x3)",
+        "config": {"workload": "varlen_causal_32seq_len256to8192_h16_d128", "sequences": len(lengths),
+                   "total_tokens": total, "max_seqlen": max_s, "H": H, "kv_heads": Hkv, "d": d,
+                   "causal": True, "padding_flops_avoided": round(1 - flops / padded, 3),
+                   "l2": "L2 flushed (512 MB write) between steps"},
+        "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / peak, 4) if peak else None,
+        "fwd_train_ms": round(ms_fwd, 4), "fwd_train_tflops": round(0.4 * flops / (ms_fwd * 1e-3) / 1e12, 2),
+        "bwd_ms": round(ms - ms_fwd, 4), "bwd_tflops": round(0.6 * flops / ((ms - ms_fwd) * 1e-3) / 1e12, 2),
+        "clocks": clk.summary(),
+    }))
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, timed on the host cores.
 
@@ -504,10 +576,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--varlen", action="store_true",
+                    help="time the step on a packed variable-length batch instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.varlen:
+        run_varlen(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

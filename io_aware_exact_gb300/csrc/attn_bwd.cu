@@ -455,7 +455,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int bkv = blockIdx.x;                  // (batch, K / V head)
     if (grid_block() >= args.num_kvblocks) return;                  // padding CTA
-    const int j = grid_block();                  // key block (causal: small j = most work)
+    int j = grid_block();                        // key block (causal: small j = most work)
     // GENERAL (grouped K / V heads and / or a packed variable-length batch): the
     // query heads of this K / V head's group, one after the other; block it of
     // the loop is query block qblk(it) of query head qhead(it), and dK_j, dV_j
@@ -478,7 +478,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             N = min(s1 - s0, args.max_seqlen);
             kvc = kvh;
             qc0 = kvh * group;
-            if (j * kTile >= N) return;                             // past this sequence
+            // causal: grid row y holds, for every sequence, the key block with
+            // num_kvblocks - y query blocks of work, so the launch order stays
+            // longest work first across sequences of different lengths
+            if (CAUSAL) j -= args.num_kvblocks - (N + kTile - 1) / kTile;
+            if (j < 0 || j * kTile >= N) return;                    // not a block of this sequence
         }
     }
     const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks == key blocks
