@@ -14,6 +14,24 @@
 
 namespace attn {
 
+// Head group size for a dense grid: the largest divisor G of `heads` whose G
+// heads' re-read bytes (bytes_per_head) fit in `budget`, raised if needed so
+// that a group still holds two waves of CTAs; 0 (plain order) when that is all
+// heads or the grid would not fit.
+int head_group_for(int heads, int blocks_per_head, long long bytes_per_head, long long budget) {
+    if (blocks_per_head > kMaxGridY || heads <= 1) return 0;
+    int g = 1;
+    for (int c = heads; c >= 1; --c)
+        if (heads % c == 0 && static_cast<long long>(c) * bytes_per_head <= budget) { g = c; break; }
+    const long long min_ctas = 2ll * device_sm_count();
+    while (g < heads && static_cast<long long>(g) * blocks_per_head < min_ctas) {
+        int c = g + 1;
+        while (heads % c != 0) ++c;
+        g = c;
+    }
+    return g >= heads ? 0 : g;
+}
+
 // Device status word written by kernels whose bounded waits run out.
 __device__ int g_status;
 
@@ -161,6 +179,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.H = H;
     a.Hkv = Hkv;
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
+    // K and V of a head are re-read by each of its query-block CTAs
+    a.head_group = head_group_for(BH, a.num_qblocks, 4ll * N * d, kFwdGroupBytes);
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_fwd(tq, tk, tv, to, to32, a, BH, d, causal != 0, bf16,
@@ -255,7 +275,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.BH = BH;
     a.H = H;
     a.Hkv = Hkv;
+    a.BHkv = B * Hkv;
     a.num_kvblocks = (N + kTile - 1) / kTile;
+    // the fp32 dQ rows and the Q, dO tiles of a head are re-read by each key-block CTA
+    a.head_group = (Hkv == H) ? head_group_for(B * H, a.num_kvblocks, 8ll * N * d, kBwdGroupBytes) : 0;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -409,6 +432,7 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* dO,
     a.BH = B * H;
     a.H = H;
     a.Hkv = Hkv;
+    a.BHkv = B * Hkv;
     a.num_kvblocks = (max_seqlen + kTile - 1) / kTile;
     a.cu_seqlens = cu_seqlens;
     a.total = total;

@@ -453,9 +453,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bkv = blockIdx.x;                  // (batch, K / V head)
-    if (grid_block() >= args.num_kvblocks) return;                  // padding CTA
+    int bkv = blockIdx.x;                        // (batch, K / V head)
     int j = grid_block();                        // key block (causal: small j = most work)
+    if (GENERAL && args.cu_seqlens != nullptr) {
+        // packed batch: head-major grid (x = key block, y / z = (sequence, K / V
+        // head)), so the key blocks of one sequence and head run together and
+        // the fp32 dQ rows they all reduce into stay in L2
+        j = blockIdx.x;
+        bkv = grid_block();
+        if (bkv >= args.BHkv) return;                               // padding CTA
+    } else if (!GENERAL && args.head_group > 0) {
+        bkv = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
+        j = blockIdx.y;
+    }
+    if (j >= args.num_kvblocks) return;                             // padding CTA
     // GENERAL (grouped K / V heads and / or a packed variable-length batch): the
     // query heads of this K / V head's group, one after the other; block it of
     // the loop is query block qblk(it) of query head qhead(it), and dK_j, dV_j
@@ -478,11 +489,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             N = min(s1 - s0, args.max_seqlen);
             kvc = kvh;
             qc0 = kvh * group;
-            // causal: grid row y holds, for every sequence, the key block with
-            // num_kvblocks - y query blocks of work, so the launch order stays
-            // longest work first across sequences of different lengths
-            if (CAUSAL) j -= args.num_kvblocks - (N + kTile - 1) / kTile;
-            if (j < 0 || j * kTile >= N) return;                    // not a block of this sequence
+            if (j * kTile >= N) return;                             // not a block of this sequence
         }
     }
     const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks == key blocks
@@ -972,7 +979,10 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const dim3 grid = lpt_grid(a.num_kvblocks, BH);
+    // packed batch: x = key block, y / z = (sequence, K / V head)
+    const dim3 grid = (GENERAL && a.cu_seqlens != nullptr) ? head_major_grid(a.num_kvblocks, BH)
+                      : (!GENERAL && a.head_group > 0) ? group_grid(a.num_kvblocks, BH, a.head_group)
+                                                      : lpt_grid(a.num_kvblocks, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
     return cudaGetLastError();
 }

@@ -29,6 +29,7 @@ struct FwdArgs {
     int H;                 // query heads
     int Hkv;               // key / value heads (H is a multiple; query head h reads K/V head h / (H / Hkv))
     int num_qblocks;       // ceil(N / 256): CTAs per head
+    int head_group;        // dense grid in head groups (x = head in group, y = block, z = group); 0: plain
     // Packed variable-length batch (nullptr: dense [B,H,N,d]): sequence b is
     // tokens [cu_seqlens[b], cu_seqlens[b+1]) of [total, H, d]; N = max_seqlen
     // then, and lse is [B, H, max_seqlen].
@@ -50,6 +51,8 @@ struct BwdArgs {
     int BH;                // batch * query heads
     int H;                 // query heads
     int Hkv;               // key / value heads (grid: batch * Hkv); query heads per group H / Hkv
+    int BHkv;              // batch * key / value heads
+    int head_group;        // dense grid in head groups (x = head in group, y = block, z = group); 0: plain
     int num_kvblocks;      // ceil(N / 128)
     // packed variable-length batch as in FwdArgs (nullptr: dense); D is then
     // [total, H] (the row order of the packed tensors), lse [B, H, max_seqlen]
@@ -104,18 +107,38 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
 cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
 
-// Grid layout shared by the attention kernels: x = (batch, head), y/z = block
-// index within a head.  Launch order is x fastest, so every head's heaviest
-// causal block is scheduled before any lighter one (longest work first).  y
-// is capped at the hardware limit and z extends it.  The index math is two
-// reads of blockIdx: the backward runs at its register limit, and a head order
-// in groups, computed with divisions in the kernel, cost it about 4%.
+// Grid layouts of the attention kernels.  Plain: x = (batch, head), y/z =
+// block index within a head.  Launch order is x fastest, so every head's
+// heaviest causal block is scheduled before any lighter one (longest work
+// first); y is capped at the hardware limit and z extends it.  The index math
+// is a few reads of blockIdx and no division: the backward runs at its
+// register limit, and a division-based mapping cost it about 4%.
 constexpr int kMaxGridY = 65535;
 
 inline dim3 lpt_grid(int blocks_per_head, int BH) {
     const int gy = blocks_per_head < kMaxGridY ? blocks_per_head : kMaxGridY;
     return dim3(BH, gy, (blocks_per_head + gy - 1) / gy);
 }
+
+// Head-major variant: x = block index within the head (0 launched first), y
+// (and z beyond 65,535) = head, so all blocks of one head run close together.
+inline dim3 head_major_grid(int blocks_per_head, int heads) {
+    const int gy = heads < kMaxGridY ? heads : kMaxGridY;
+    return dim3(blocks_per_head, gy, (heads + gy - 1) / gy);
+}
+
+// Head groups: x = head within a group of G heads, y = block rank, z = group,
+// so the blocks of G heads run together, longest work first within the group.
+// Needs G to divide the head count and blocks_per_head <= 65,535.
+inline dim3 group_grid(int blocks_per_head, int heads, int G) {
+    return dim3(G, blocks_per_head, heads / G);
+}
+
+// Re-read bytes a head group may hold (L2 is 126 MB): measured on the causal
+// B=2 H=16 N=8192 d=128 workload, groups of 8 heads beat 2, 4, 16 and all 32.
+constexpr long long kFwdGroupBytes = 32ll << 20;
+constexpr long long kBwdGroupBytes = 64ll << 20;
+int head_group_for(int heads, int blocks_per_head, long long bytes_per_head, long long budget);
 
 // Block index within the head (0 = first launched); >= blocks_per_head only
 // for padding CTAs of the last z-slice.

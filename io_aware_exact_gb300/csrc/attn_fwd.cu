@@ -81,10 +81,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;                                     // (batch, query head)
-    if (grid_block() >= args.num_qblocks) return;                  // padding CTA
-    const int qb = args.num_qblocks - 1 - grid_block();            // heavy blocks first
-    const int q0 = qb * (C::TILES * kTile);
+    // Dense: x = (batch, query head), y / z = block rank.  Packed batch:
+    // head-major, x = block rank, y / z = (sequence, query head), so the CTAs
+    // of one sequence and head, which re-read the same K / V, run together.
+    int bh = VARLEN ? grid_block() : static_cast<int>(blockIdx.x);
+    int rank = VARLEN ? static_cast<int>(blockIdx.x) : grid_block();
+    if (!VARLEN && args.head_group > 0) {
+        bh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
+        rank = blockIdx.y;
+    }
+    if (rank >= args.num_qblocks || (VARLEN && bh >= args.BH)) return;   // padding CTA
+    int qb = args.num_qblocks - 1 - rank;                          // heavy blocks first
     // TMA coordinates: the rows of this sequence start at tok0, the head
     // coordinate is hq for Q / O and hk for K / V.  Dense [B,H,N,d]: tok0 = 0
     // and the head coordinate is the (batch, head) index.  Packed variable
@@ -99,8 +106,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         N = min(s1 - s0, args.max_seqlen);
         hq = h;
         hk = h / (args.H / args.Hkv);
-        if (q0 >= N) return;                                       // past this sequence
+        qb = (N + C::TILES * kTile - 1) / (C::TILES * kTile) - 1 - rank;
+        if (qb < 0) return;                                        // past this sequence
     }
+    const int q0 = qb * (C::TILES * kTile);
     const int nkv_all = (N + kTile - 1) / kTile;
     int nkv[2];
 #pragma unroll
@@ -487,7 +496,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const dim3 grid = lpt_grid(a.num_qblocks, BH);
+    const dim3 grid = VARLEN ? head_major_grid(a.num_qblocks, BH)
+                      : a.head_group > 0 ? group_grid(a.num_qblocks, BH, a.head_group)
+                                         : lpt_grid(a.num_qblocks, BH);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, to32, a);
     return cudaGetLastError();
 }
