@@ -2,9 +2,12 @@
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
 ``cpu_baseline`` / reference leg may import this package.  It shares no code
-with the CUDA library in ``io_aware_exact_gb300``: the arithmetic lives in
-``attn_oracle.c`` (plain C, fp64), built by :func:`build` with the host
-compiler, and this module only marshals numpy arrays into it.
+with the CUDA library in ``io_aware_exact_gb300``.  The dense functions'
+arithmetic lives in ``attn_oracle.c`` (plain C, fp64), built by :func:`build`
+with the host compiler, and this module only marshals numpy arrays into it;
+the functions with an explicit visibility mask (block-sparse layouts) are
+written here with numpy fp64 matrix products, the same definitions with
+dropped scores excluded from the softmax.
 
 The functions follow, one head at a time:
 
@@ -263,3 +266,77 @@ def attention_backward_varlen(q, k, v, dO, cu_seqlens, causal: bool, scale: floa
             dk[s0:s1, g] += dkb
             dv[s0:s1, g] += dvb
     return dq, dk, dv
+
+
+def expand_block_mask(block_mask, nq: int, nk: int, block: int, causal: bool) -> np.ndarray:
+    """Element visibility [nq, nk] (True = key j enters row i's softmax) of a
+    block-sparse layout: block_mask [ceil(nq / block), ceil(nk / block)], a
+    nonzero entry keeps the block x block tile of scores, a zero entry drops
+    it (sj-techlog "FlashAttention 원 논문 해부", section "대안, 비교와 선택
+    기준": block-sparse FlashAttention skips the zero blocks of a block mask
+    fixed in advance).  With ``causal`` the top-left causal mask applies on
+    top (j <= i)."""
+    bm = np.asarray(block_mask) != 0
+    assert bm.shape == ((nq + block - 1) // block, (nk + block - 1) // block)
+    vis = np.repeat(np.repeat(bm, block, axis=0), block, axis=1)[:nq, :nk]
+    if causal:
+        vis = vis & (np.arange(nk)[None, :] <= np.arange(nq)[:, None])
+    return vis
+
+
+def attention_forward_masked(q, k, v, visible, scale: float):
+    """O [nq, dv] and lse [nq] of one head with an explicit visibility mask.
+
+    S = tau Q K^T with invisible scores excluded, P the row softmax over the
+    visible keys (row maximum subtracted), O = P V, lse_i = m_i + ln sum_j
+    exp(s_ij - m_i) (same definitions as the rest of this module).  A row with
+    no visible key has an empty softmax (the sj-techlog page's all-masked-row
+    case, "값을 하나 바꾸는 경계 실험"); the reading taken is O = 0 and
+    lse = -inf, the limit of a row whose keys all contribute nothing."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    vis = np.asarray(visible, dtype=bool)
+    s = scale * (q @ k.T)
+    s = np.where(vis, s, -np.inf)
+    has = vis.any(axis=1)
+    m = np.where(has, s.max(axis=1), 0.0)
+    e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    z = e.sum(axis=1)
+    p = np.where(has[:, None], e / np.where(has, z, 1.0)[:, None], 0.0)
+    lse = np.where(has, m + np.log(np.where(has, z, 1.0)), -np.inf)
+    return p @ v, lse
+
+
+def attention_backward_masked(q, k, v, dO, visible, scale: float):
+    """(dQ, dK, dV, lse, D) of one head with an explicit visibility mask:
+    the analytic backward of the FlashAttention-2 review ("Backward Pass"),
+    dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij, dS = P o (dP - D),
+    dQ = tau dS K, dK = tau dS^T Q, with P = 0 on invisible entries.  Rows
+    with no visible key contribute nothing."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    vis = np.asarray(visible, dtype=bool)
+    s = np.where(vis, scale * (q @ k.T), -np.inf)
+    has = vis.any(axis=1)
+    m = np.where(has, s.max(axis=1), 0.0)
+    e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    z = np.where(has, e.sum(axis=1), 1.0)
+    p = e / z[:, None]
+    lse = np.where(has, m + np.log(z), -np.inf)
+    dv = p.T @ dO
+    dp = dO @ v.T
+    D = (p * dp).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), dv, lse, D
+
+
+def attention_forward_block_sparse(q, k, v, block_mask, causal: bool, scale: float,
+                                   block: int = 128):
+    """O, lse of one head under a block-sparse layout (see expand_block_mask)."""
+    vis = expand_block_mask(block_mask, len(q), len(k), block, causal)
+    return attention_forward_masked(q, k, v, vis, scale)
+
+
+def attention_backward_block_sparse(q, k, v, dO, block_mask, causal: bool, scale: float,
+                                    block: int = 128):
+    """(dQ, dK, dV, lse, D) of one head under a block-sparse layout."""
+    vis = expand_block_mask(block_mask, len(q), len(k), block, causal)
+    return attention_backward_masked(q, k, v, dO, vis, scale)

@@ -395,3 +395,112 @@ def test_varlen_backward_matches_finite_differences():
                       (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
         scale = max(1.0, np.max(np.abs(want)))
         assert np.max(np.abs(got - want)) / scale < 1e-6
+
+
+# --------------------------------------------------------------------------
+# Block-sparse layouts (numpy fp64 functions of the oracle)
+# --------------------------------------------------------------------------
+
+def _visible_keys_by_hand(bm, i, nk, block, causal):
+    return [j for j in range(nk) if bm[i // block][j // block] and (not causal or j <= i)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_rows_match_attention_over_their_keys(causal):
+    """Every row of the block-sparse forward equals plain attention (the C
+    oracle) of that query over exactly the keys its blocks keep, listed by
+    hand; a row whose blocks are all dropped gives O = 0 and lse = -inf.  An
+    asymmetric mask with a ragged last block catches a transposed mask, an
+    off-by-one block index and a lost causal mask."""
+    r = _rng(80 + int(causal))
+    nq = nk = 11
+    block, d, dv, tau = 3, 3, 2, 0.7
+    bm = np.array([[1, 0, 0, 1], [1, 1, 0, 0], [0, 0, 0, 0], [0, 1, 1, 1]], np.uint8)
+    q, k, v = r.normal(size=(nq, d)), r.normal(size=(nk, d)), r.normal(size=(nk, dv))
+    o, lse = oracle.attention_forward_block_sparse(q, k, v, bm, causal, tau, block=block)
+    for i in range(nq):
+        sel = _visible_keys_by_hand(bm, i, nk, block, causal)
+        if not sel:
+            assert np.all(o[i] == 0.0) and lse[i] == -np.inf
+            continue
+        oi, li = oracle.attention_forward(q[i:i + 1], k[sel], v[sel], False, tau)
+        assert np.max(np.abs(o[i] - oi[0])) < 1e-13
+        assert abs(lse[i] - li[0]) < 1e-13
+    assert np.all(o[6:9] == 0.0)                 # query block 2 keeps no key block
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_full_mask_is_dense_attention(causal):
+    """An all-ones block mask leaves plain (causal) attention, forward and
+    backward, as the C oracle computes it."""
+    r = _rng(82 + int(causal))
+    n, block, tau = 10, 4, 0.6
+    q, k, v, dO = (r.normal(size=(n, 3)) for _ in range(4))
+    bm = np.ones((3, 3), np.uint8)
+    o, lse = oracle.attention_forward_block_sparse(q, k, v, bm, causal, tau, block=block)
+    o2, lse2 = oracle.attention_forward(q, k, v, causal, tau)
+    assert np.max(np.abs(o - o2)) < 1e-13 and np.max(np.abs(lse - lse2)) < 1e-13
+    got = oracle.attention_backward_block_sparse(q, k, v, dO, bm, causal, tau, block=block)
+    want = oracle.attention_backward(q, k, v, dO, causal, tau)
+    for a, b in zip(got, want):
+        assert np.max(np.abs(a - b)) < 1e-12
+
+
+def test_block_sparse_diagonal_mask_is_independent_blocks():
+    """A block-diagonal mask is attention within each block: the C oracle
+    run on each block's slice alone (the last block ragged), forward and
+    backward."""
+    r = _rng(84)
+    n, block, tau = 10, 4, 0.8
+    q, k, v, dO = (r.normal(size=(n, 2)) for _ in range(4))
+    bm = np.eye(3, dtype=np.uint8)
+    o, lse = oracle.attention_forward_block_sparse(q, k, v, bm, False, tau, block=block)
+    dq, dk, dv, _, _ = oracle.attention_backward_block_sparse(q, k, v, dO, bm, False, tau,
+                                                              block=block)
+    for s0 in range(0, n, block):
+        sl = slice(s0, min(n, s0 + block))
+        ob, lb = oracle.attention_forward(q[sl], k[sl], v[sl], False, tau)
+        gq, gk, gv, _, _ = oracle.attention_backward(q[sl], k[sl], v[sl], dO[sl], False, tau)
+        for a, b in ((o[sl], ob), (lse[sl], lb), (dq[sl], gq), (dk[sl], gk), (dv[sl], gv)):
+            assert np.max(np.abs(a - b)) < 1e-12
+
+
+def test_block_sparse_dropped_keys_do_not_matter():
+    """Keys and values in key blocks that no query block keeps can be
+    anything: outputs unchanged, and their dK, dV are exactly zero."""
+    r = _rng(86)
+    n, block, tau = 9, 3, 0.7
+    bm = np.array([[1, 0, 1], [1, 0, 0], [0, 0, 1]], np.uint8)  # key block 1 dropped
+    q, k, v, dO = (r.normal(size=(n, 3)) for _ in range(4))
+    k2, v2 = k.copy(), v.copy()
+    k2[3:6] = 50 * r.normal(size=(3, 3))
+    v2[3:6] = r.normal(size=(3, 3))
+    a = oracle.attention_forward_block_sparse(q, k, v, bm, True, tau, block=block)
+    b = oracle.attention_forward_block_sparse(q, k2, v2, bm, True, tau, block=block)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    _, dk, dv, _, _ = oracle.attention_backward_block_sparse(q, k, v, dO, bm, True, tau,
+                                                             block=block)
+    assert np.all(dk[3:6] == 0.0) and np.all(dv[3:6] == 0.0)
+
+
+def test_block_sparse_backward_matches_finite_differences():
+    """Central differences of L = sum(dO * O) for the block-sparse forward,
+    causal, with an empty query block (its dQ must be zero); d != dv."""
+    r = _rng(88)
+    n, block, tau = 8, 3, 0.7
+    bm = np.array([[1, 0, 1], [0, 0, 0], [1, 1, 1]], np.uint8)
+    q, k = r.normal(size=(n, 3)), r.normal(size=(n, 3))
+    v, dO = r.normal(size=(n, 2)), r.normal(size=(n, 2))
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward_block_sparse(qq, kk, vv, bm, True, tau, block=block)
+        return float(np.sum(o * dO))
+
+    dq, dk, dv, _, D = oracle.attention_backward_block_sparse(q, k, v, dO, bm, True, tau,
+                                                              block=block)
+    for got, want in ((dq, _fd_grad(q, lambda x: loss(x, k, v))),
+                      (dk, _fd_grad(k, lambda x: loss(q, x, v))),
+                      (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
+    assert np.all(dq[3:6] == 0.0) and np.all(D[3:6] == 0.0)
