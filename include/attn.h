@@ -25,7 +25,7 @@
  *    16-byte aligned.  The caller allocates and owns every buffer; the library
  *    allocates no device memory and keeps no per-call state.
  *  - Sizes: B, H, N >= 1; d is 64 or 128; B*H <= 2^31-1; B*H*N*d < 2^62;
- *    N <= 2^24.  scale must be finite and > 0 (callers usually pass
+ *    N <= 2^24 - 256.  scale must be finite and > 0 (callers usually pass
  *    1/sqrt(d)).
  *  - Causal masking is top-left aligned: key j is visible to query i iff
  *    j <= i.  Every query row therefore sees at least key 0.
@@ -74,10 +74,11 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
  * Forward pass for training: as attn_fwd, and additionally writes o32
  * [B,H,N,d] fp32, the same O before its rounding to 16 bits, for
  * attn_bwd_preprocess_o32 (the backward saves O, sj-techlog page, backward
- * section; here at accumulation precision).  In both forward entry points
- * each output row is normalised by the sum of the probabilities as rounded
- * for the P V product, so its weights sum to exactly 1; lse uses the exact
- * fp32 sum.  o32 must be non-NULL and 16-byte aligned.
+ * section; here at accumulation precision).  Here each output row (o32 and
+ * o) is normalised by the sum of the probabilities as rounded for the P V
+ * product, so its weights sum to exactly 1; attn_fwd normalises by the exact
+ * fp32 sum, so the two 16-bit outputs may differ in the last bit.  lse uses
+ * the exact fp32 sum in both.  o32 must be non-NULL and 16-byte aligned.
  */
 int attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
                    int B, int H, int N, int d, int causal, float scale, void* stream);
@@ -257,6 +258,53 @@ int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void*
                         void* dq, void* dk, void* dv, const int* cu_seqlens,
                         int B, int total, int max_seqlen, int H, int Hkv, int d, int causal,
                         float scale, void* stream);
+
+/*
+ * Block-sparse layouts.  The sj-techlog page (section "대안, 비교와 선택
+ * 기준") describes block-sparse FlashAttention: a block mask fixed in advance,
+ * whose zero blocks are skipped.  Here the block is one 128 x 128 tile:
+ *  - block_mask: device bytes, one per (query block r, key block c) with
+ *    Nb = ceil(N / 128) blocks per side, row-major [Nb, Nb]; nonzero keeps the
+ *    tile, zero drops it (its scores leave the softmax, as if -inf).  Head
+ *    (b, h) reads the mask at block_mask + (b * H + h) * mask_head_stride;
+ *    mask_head_stride = 0 shares one mask between all heads, otherwise it
+ *    must be >= Nb * Nb.  The causal mask, if requested, applies on top.
+ *  - A query row whose kept tiles hold no visible key has an empty softmax:
+ *    its O row is 0, its lse -inf, and it contributes no gradient.  A key
+ *    block that no query block keeps gets dK = dV = 0.
+ *  - Dense [B,H,N,d] layout with one K / V head per query head (no grouped
+ *    heads, no packed batches); N <= 49,152 (384 blocks).  Other arguments
+ *    and errors as for attn_fwd / attn_fwd_train / attn_bwd; a bad mask
+ *    argument returns ATTN_ERR_INVALID_ARG with nothing enqueued.
+ *  - The training path is attn_fwd_train_bsparse, attn_bwd_preprocess_o32
+ *    (D = rowsum(dO o O) from the fp32 O already holds only the kept tiles),
+ *    then attn_bwd_bsparse with the same mask.  attn_bwd_preprocess (D from
+ *    recomputed dense tiles) does not apply to a sparse layout.
+ *  - Work and memory traffic scale with the number of kept tiles: a CTA
+ *    lists its kept tiles in shared memory at start and visits only those
+ *    (the forward's two query tiles per CTA visit the union of their kept
+ *    key blocks; a tile that drops a listed block gives it P = 0).
+ */
+int attn_fwd_bsparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const void* block_mask, long long mask_head_stride, int B, int H, int N,
+                     int d, int causal, float scale, void* stream);
+int attn_fwd_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const void* block_mask, long long mask_head_stride, int B, int H, int N,
+                         int d, int causal, float scale, void* stream);
+int attn_fwd_train_bsparse(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, const void* block_mask, long long mask_head_stride, int B,
+                           int H, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_train_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                               float* lse, const void* block_mask, long long mask_head_stride,
+                               int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_bsparse(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                     void* dv, const void* block_mask, long long mask_head_stride, int B, int H,
+                     int N, int d, int causal, float scale, void* stream);
+int attn_bwd_bsparse_f16(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                         void* dv, const void* block_mask, long long mask_head_stride, int B,
+                         int H, int N, int d, int causal, float scale, void* stream);
 
 /* Static English description of a status code. */
 const char* attn_status_string(int status);

@@ -87,6 +87,18 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = at
                 fn.restype = I
+            # block-sparse layouts: (block_mask, mask_head_stride) before B
+            LL = ctypes.c_longlong
+            sfwd = [P, P, P, P, P, P, LL, I, I, I, I, I, F, P]
+            sfwdt = [P, P, P, P, P, P, P, LL, I, I, I, I, I, F, P]
+            sbwd = [P, P, P, P, P, P, P, P, P, P, P, LL, I, I, I, I, I, F, P]
+            for name, at in (("attn_fwd_bsparse", sfwd), ("attn_fwd_bsparse_f16", sfwd),
+                             ("attn_fwd_train_bsparse", sfwdt),
+                             ("attn_fwd_train_bsparse_f16", sfwdt),
+                             ("attn_bwd_bsparse", sbwd), ("attn_bwd_bsparse_f16", sbwd)):
+                fn = getattr(L, name)
+                fn.argtypes = at
+                fn.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -159,6 +171,26 @@ def attn_bwd(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, N, d, causal, scal
     fn, hs = _heads("attn_bwd", f16, H, Hkv)
     _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, *hs, N, d, int(bool(causal)),
               float(scale), stream), "attn_bwd")
+
+
+def attn_fwd_bsparse(q, k, v, o, lse, block_mask, mask_head_stride, B, H, N, d, causal, scale,
+                     stream, f16=False, o32=None):
+    """Block-sparse forward; with ``o32`` the training variant (also writes O in fp32)."""
+    if o32 is None:
+        fn = lib().attn_fwd_bsparse_f16 if f16 else lib().attn_fwd_bsparse
+        _check(fn(q, k, v, o, lse, block_mask, int(mask_head_stride), B, H, N, d,
+                  int(bool(causal)), float(scale), stream), "attn_fwd_bsparse")
+    else:
+        fn = lib().attn_fwd_train_bsparse_f16 if f16 else lib().attn_fwd_train_bsparse
+        _check(fn(q, k, v, o, o32, lse, block_mask, int(mask_head_stride), B, H, N, d,
+                  int(bool(causal)), float(scale), stream), "attn_fwd_train_bsparse")
+
+
+def attn_bwd_bsparse(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, block_mask, mask_head_stride,
+                     B, H, N, d, causal, scale, stream, f16=False):
+    fn = lib().attn_bwd_bsparse_f16 if f16 else lib().attn_bwd_bsparse
+    _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, block_mask, int(mask_head_stride),
+              B, H, N, d, int(bool(causal)), float(scale), stream), "attn_bwd_bsparse")
 
 
 def attn_get_device_status(stream=None) -> int:
@@ -263,6 +295,62 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
     attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
              B, H, N, d, causal, scale, s, f16, Hkv)
+    return dq, dk, dv
+
+
+def _block_mask_arg(block_mask, B, H, N):
+    """(pointer, per-head stride) of a uint8 CUDA block mask [Nb, Nb] (one mask
+    for every head) or [B, H, Nb, Nb], Nb = ceil(N / 128)."""
+    torch = _torch()
+    nb = (N + 127) // 128
+    if block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous():
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor")
+    if tuple(block_mask.shape) == (nb, nb):
+        return block_mask.data_ptr(), 0
+    if tuple(block_mask.shape) == (B, H, nb, nb):
+        return block_mask.data_ptr(), nb * nb
+    raise ValueError("block_mask must be [Nb, Nb] or [B, H, Nb, Nb] with Nb = ceil(N / 128)")
+
+
+def forward_bsparse(q, k, v, block_mask, causal: bool = False, scale=None, o=None, lse=None,
+                    o32=None, stream=None):
+    """Block-sparse forward over [B,H,N,d] tensors: 128 x 128 tiles whose
+    block_mask byte is zero are dropped.  With ``o32`` (fp32 [B,H,N,d], or True)
+    the training variant, returning (o, lse, o32); else (o, lse)."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else float(scale)
+    mp, ms = _block_mask_arg(block_mask, B, H, N)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if o32 is True:
+        o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    attn_fwd_bsparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), mp,
+                     ms, B, H, N, d, causal, scale, _stream_handle(stream), f16,
+                     None if o32 is None else o32.data_ptr())
+    return (o, lse) if o32 is None else (o, lse, o32)
+
+
+def backward_bsparse(q, k, v, o32, lse, dO, block_mask, causal: bool = False, scale=None,
+                     dq=None, dk=None, dv=None, D=None, dq_accum=None, stream=None):
+    """dQ, dK, dV of the block-sparse forward: D from the fp32 O of
+    forward_bsparse(..., o32=True), then the backward over the kept tiles."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v, dO)
+    scale = d ** -0.5 if scale is None else float(scale)
+    mp, ms = _block_mask_arg(block_mask, B, H, N)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    D = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if D is None else D
+    if dq_accum is None:
+        dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    s = _stream_handle(stream)
+    attn_bwd_preprocess_o32(o32.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(),
+                            B, H, N, d, s, f16)
+    attn_bwd_bsparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                     D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                     dv.data_ptr(), mp, ms, B, H, N, d, causal, scale, s, f16)
     return dq, dk, dv
 
 

@@ -40,6 +40,9 @@ namespace {
 // try_wait polls before a bounded wait gives up: an unsuccessful poll suspends
 // the thread for about 2 us, so this is about 2 s.
 constexpr unsigned int kDefaultWaitPolls = 1000000u;
+// Longest dense sequence: the forward's grid holds at most 65,535 blocks of
+// 256 query rows in one dimension.
+constexpr int kMaxN = (1 << 24) - 256;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -99,7 +102,7 @@ int check_shape(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEAD_DIM;
     if (static_cast<long long>(B) * H > 2147483647LL) return ATTN_ERR_INVALID_ARG;
-    if (N > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    if (N > kMaxN) return ATTN_ERR_INVALID_ARG;
     return ATTN_OK;
 }
 
@@ -146,14 +149,27 @@ int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
 
 int map_launch(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
 
+// Block-sparse layout checks: a mask is given, one query head per K / V
+// head, N within the shared-memory list, and per-head masks (stride > 0) do
+// not overlap.
+int check_sparse(const void* block_mask, long long mask_stride, int H, int Hkv, int N) {
+    if (!block_mask || H != Hkv || N > kMaxSparseBlocks * kTile || mask_stride < 0)
+        return ATTN_ERR_INVALID_ARG;
+    const long long nb = (N + kTile - 1) / kTile;
+    if (mask_stride != 0 && mask_stride < nb * nb) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse, int B,
-             int H, int Hkv, int N, int d, int causal, float scale, void* stream, bool bf16) {
+             int H, int Hkv, int N, int d, int causal, float scale, void* stream, bool bf16,
+             const void* block_mask = nullptr, long long mask_stride = 0) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (o32 != nullptr && !aligned16(o32)) return ATTN_ERR_MISALIGNED;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
     if ((rc = check_kv_heads(H, Hkv))) return rc;
     if ((rc = check_scale(scale))) return rc;
+    if (block_mask != nullptr && (rc = check_sparse(block_mask, mask_stride, H, Hkv, N))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
@@ -181,6 +197,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.num_qblocks = (N + 2 * kTile - 1) / (2 * kTile);
     // K and V of a head are re-read by each of its query-block CTAs
     a.head_group = head_group_for(BH, a.num_qblocks, 4ll * N * d, kFwdGroupBytes);
+    a.block_mask = static_cast<const uint8_t*>(block_mask);
+    a.mask_head_stride = mask_stride;
+    a.mask_cols = (N + kTile - 1) / kTile;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_fwd(tq, tk, tv, to, to32, a, BH, d, causal != 0, bf16,
@@ -241,13 +260,15 @@ int pre_o32_impl(const float* o32, const void* dO, float* D, float* dq_accum, in
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
              const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int Hkv,
-             int N, int d, int causal, float scale, void* stream, bool bf16) {
+             int N, int d, int causal, float scale, void* stream, bool bf16,
+             const void* block_mask = nullptr, long long mask_stride = 0) {
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
     if (rc) return rc;
     if ((rc = check_kv_heads(H, Hkv))) return rc;
     if ((rc = check_scale(scale))) return rc;
+    if (block_mask != nullptr && (rc = check_sparse(block_mask, mask_stride, H, Hkv, N))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
         !aligned16(D) || !aligned16(dq_accum) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv))
@@ -279,6 +300,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.num_kvblocks = (N + kTile - 1) / kTile;
     // the fp32 dQ rows and the Q, dO tiles of a head are re-read by each key-block CTA
     a.head_group = (Hkv == H) ? head_group_for(B * H, a.num_kvblocks, 8ll * N * d, kBwdGroupBytes) : 0;
+    a.block_mask = static_cast<const uint8_t*>(block_mask);
+    a.mask_head_stride = mask_stride;
+    a.mask_cols = a.num_kvblocks;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -581,6 +605,58 @@ int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO
                      void* stream) {
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
                     stream, false);
+}
+
+int attn_fwd_bsparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const void* block_mask, long long mask_head_stride, int B, int H, int N,
+                     int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, true,
+                    block_mask, mask_head_stride);
+}
+
+int attn_fwd_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const void* block_mask, long long mask_head_stride, int B, int H, int N,
+                         int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, false,
+                    block_mask, mask_head_stride);
+}
+
+int attn_fwd_train_bsparse(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, const void* block_mask, long long mask_head_stride, int B,
+                           int H, int N, int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true,
+                    block_mask, mask_head_stride);
+}
+
+int attn_fwd_train_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                               float* lse, const void* block_mask, long long mask_head_stride,
+                               int B, int H, int N, int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false,
+                    block_mask, mask_head_stride);
+}
+
+int attn_bwd_bsparse(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                     void* dv, const void* block_mask, long long mask_head_stride, int B, int H,
+                     int N, int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
+                    stream, true, block_mask, mask_head_stride);
+}
+
+int attn_bwd_bsparse_f16(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                         void* dv, const void* block_mask, long long mask_head_stride, int B,
+                         int H, int N, int d, int causal, float scale, void* stream) {
+    if (!block_mask) return ATTN_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
+                    stream, false, block_mask, mask_head_stride);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -409,13 +409,16 @@ struct BwdCfg {
     // shared-memory window starting 1024-byte aligned (checked at run time).
     static constexpr int SLACK = (D == 128) ? 0 : 1024;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + SLACK;
+    // block-sparse variant: the key block's list of kept query blocks
+    static constexpr int LIST_OFF = MISC_OFF + 16;
+    static constexpr int SMEM_SPARSE = LIST_OFF + 2 * kMaxSparseBlocks + SLACK;
     static constexpr int THREADS = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0, P_COL = 0, DP_COL = 128, DS_COL = 128, DQ_COL = 128;
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
     static constexpr int DQ_BOX_COLS = 32;                  // fp32 columns per reduce box
     static constexpr int DQ_BOX_BYTES = kTile * DQ_BOX_COLS * 4;   // 16 KB
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SMEM_SPARSE <= 232448, "shared memory budget");
     static_assert(D * kTile * 4 <= 2 * TILE_BYTES, "dQ staging fits in the Q_i + dO_i tiles");
 };
 
@@ -429,7 +432,7 @@ __device__ __forceinline__ uint32_t dq_box_addr(uint32_t sbase, int s, int b) {
            (b % per_tile) * C::DQ_BOX_BYTES;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GENERAL>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -453,18 +456,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int bkv = blockIdx.x;                        // (batch, K / V head)
-    int j = grid_block();                        // key block (causal: small j = most work)
-    if (GENERAL && args.cu_seqlens != nullptr) {
-        // packed batch: head-major grid (x = key block, y / z = (sequence, K / V
-        // head)), so the key blocks of one sequence and head run together and
-        // the fp32 dQ rows they all reduce into stay in L2
-        j = blockIdx.x;
-        bkv = grid_block();
-        if (bkv >= args.BHkv) return;                               // padding CTA
-    } else if (!GENERAL && args.head_group > 0) {
+    // (batch, K / V head) and key block (causal: small j = most work).  Dense
+    // MHA: head groups, x = head within the group, y = key block, z = group
+    // (one group of all heads is the plain order).  Otherwise x = (batch, K / V
+    // head) and y / z = key block, or, for a packed batch, head-major: x = key
+    // block and y / z = (sequence, K / V head), so the key blocks of one
+    // sequence and head run together and the fp32 dQ rows they all reduce into
+    // stay in L2.
+    int bkv, j;
+    if constexpr (!GENERAL) {
         bkv = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
         j = blockIdx.y;
+    } else {
+        bkv = blockIdx.x;
+        j = grid_block();
+        if (args.cu_seqlens != nullptr) {
+            j = blockIdx.x;
+            bkv = grid_block();
+            if (bkv >= args.BHkv) return;                           // padding CTA
+        }
     }
     if (j >= args.num_kvblocks) return;                             // padding CTA
     // GENERAL (grouped K / V heads and / or a packed variable-length batch): the
@@ -495,10 +505,29 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks == key blocks
     const int i_start = CAUSAL ? j : 0;
     const int n_i = nq - i_start;                // query blocks per query head
-    const int n_it = group * n_i;
+    int n_it = group * n_i;
+    // Block-sparse layout (dense, one query head per CTA): the query blocks
+    // visited are those whose tile with key block j is kept, in order, listed
+    // by warp 3 before the roles start.
+    const uint16_t* blist = reinterpret_cast<const uint16_t*>(smem + C::LIST_OFF);
+    if (SPARSE && warp == 3) {
+        const uint8_t* mcol = args.block_mask + bkv * args.mask_head_stride + j;
+        uint16_t* wl = reinterpret_cast<uint16_t*>(smem + C::LIST_OFF);
+        int n = 0;
+        for (int c0 = i_start; c0 < nq; c0 += 32) {
+            const int i = c0 + lane;
+            const bool keep = i < nq && mcol[static_cast<long long>(i) * args.mask_cols] != 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, keep);
+            if (keep) wl[n + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(i);
+            n += __popc(bal);
+        }
+        if (lane == 0) *reinterpret_cast<int*>(smem + C::MISC_OFF + 8) = n;
+    }
     auto qhead = [&](int it) { return GENERAL ? qc0 + it / n_i : qc0; };
     auto qflat = [&](int it) { return GENERAL ? qf0 + it / n_i : qf0; };
-    auto qblk = [&](int it) { return GENERAL ? i_start + it % n_i : i_start + it; };
+    auto qblk = [&](int it) -> int {
+        return SPARSE ? static_cast<int>(blist[it]) : GENERAL ? i_start + it % n_i : i_start + it;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_KVFULL), 1);
@@ -540,7 +569,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, args.status, args.wait_polls};
-    const bool skip = *abort_flag != 0;
+    bool skip = *abort_flag != 0;
+    if constexpr (SPARSE) {
+        n_it = *reinterpret_cast<const int*>(smem + C::MISC_OFF + 8);
+        if (n_it == 0 && !skip) {
+            // no query block keeps a tile with these keys: dK = dV = 0
+            const int rows = min(kTile, N - j * kTile);
+            const size_t base = (static_cast<size_t>(bkv) * N + static_cast<size_t>(j) * kTile) * D;
+            for (int e = threadIdx.x; e < rows * (D / 8); e += C::THREADS) {
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.dk) + base)[e] = make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.dv) + base)[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (n_it == 0) skip = true;
+    }
 
     // Register budgets: 384 threads x 168 registers at launch; the role warps
     // (TMA, MMA, dQ reducer, lse/D loader) need few, the two compute
@@ -970,20 +1012,20 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GENERAL>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE = false>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                                 const CUtensorMap& tdv, const BwdArgs& a, int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GENERAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GENERAL, SPARSE>;
+    constexpr int smem = SPARSE ? C::SMEM_SPARSE : C::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // packed batch: x = key block, y / z = (sequence, K / V head)
-    const dim3 grid = (GENERAL && a.cu_seqlens != nullptr) ? head_major_grid(a.num_kvblocks, BH)
-                      : (!GENERAL && a.head_group > 0) ? group_grid(a.num_kvblocks, BH, a.head_group)
-                                                      : lpt_grid(a.num_kvblocks, BH);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
+    const dim3 grid = !GENERAL ? group_grid(a.num_kvblocks, BH, a.head_group > 0 ? a.head_group : BH)
+                      : a.cu_seqlens != nullptr ? head_major_grid(a.num_kvblocks, BH)
+                                                : lpt_grid(a.num_kvblocks, BH);
+    kern<<<grid, C::THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
     return cudaGetLastError();
 }
 
@@ -1022,10 +1064,14 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
                        bool bf16, cudaStream_t stream) {
-    const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr;
+    // the dense MHA kernel's head-group grid holds at most 65,535 key blocks
+    const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr || a.num_kvblocks > kMaxGridY;
+    const bool sparse = a.block_mask != nullptr;   // dense layout, Hkv = H only
+    if (sparse && general) return cudaErrorInvalidValue;
 #define ATTN_BWD_CASE(D_, C_, B_)                                                              \
     if (d == D_ && causal == C_ && bf16 == B_)                                                 \
-        return general ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+        return sparse ? launch_bwd_t<D_, C_, B_, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+             : general ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
                        : launch_bwd_t<D_, C_, B_, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)
     ATTN_BWD_CASE(64, true, true)

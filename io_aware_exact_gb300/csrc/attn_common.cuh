@@ -19,6 +19,10 @@ constexpr int kTile = 128;
 constexpr int kBoxCols = 64;
 constexpr int kBoxBytes = kTile * kBoxCols * 2;  // 16 KB
 
+// Block-sparse layouts: a CTA lists the tiles it keeps in shared memory, at
+// most this many (N <= 384 * 128 = 49,152); list entries are 16-bit.
+constexpr int kMaxSparseBlocks = 384;
+
 struct FwdArgs {
     void* o;               // [B*H, N, d] 16-bit, written
     float* o32;            // [B*H, N, d] fp32 copy of O for the backward, or nullptr
@@ -36,6 +40,12 @@ struct FwdArgs {
     const int* cu_seqlens;
     int total;
     int max_seqlen;
+    // Block-sparse layout (nullptr: none): one byte per 128 x 128 tile
+    // (query block, key block) at block_mask + bh * mask_head_stride, row-major
+    // with mask_cols = ceil(N / 128) columns; zero drops the tile.
+    const uint8_t* block_mask;
+    long long mask_head_stride;
+    int mask_cols;
     float scale_log2;      // softmax scale * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
@@ -59,6 +69,10 @@ struct BwdArgs {
     const int* cu_seqlens;
     int total;
     int max_seqlen;
+    // block-sparse layout as in FwdArgs (nullptr: none)
+    const uint8_t* block_mask;
+    long long mask_head_stride;
+    int mask_cols;
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)

@@ -57,15 +57,18 @@ struct FwdCfg {
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + runtime alignment slack
+    // block-sparse variant: the CTA's list of kept key blocks after the misc words
+    static constexpr int LIST_OFF = MISC_OFF + 16;
+    static constexpr int SMEM_SPARSE = LIST_OFF + 2 * kMaxSparseBlocks + 1024;
     static constexpr int THREADS = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns: S/P of tile t at 128*t, O of tile t at 256 + D*t.
     __device__ static constexpr uint32_t s_col(int t) { return 128u * t; }
     __device__ static constexpr uint32_t o_col(int t) { return 256u + D * t; }
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SMEM_SPARSE <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -81,15 +84,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Dense: x = (batch, query head), y / z = block rank.  Packed batch:
-    // head-major, x = block rank, y / z = (sequence, query head), so the CTAs
-    // of one sequence and head, which re-read the same K / V, run together.
-    int bh = VARLEN ? grid_block() : static_cast<int>(blockIdx.x);
-    int rank = VARLEN ? static_cast<int>(blockIdx.x) : grid_block();
-    if (!VARLEN && args.head_group > 0) {
-        bh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
-        rank = blockIdx.y;
-    }
+    // Dense: head groups, x = head within the group, y = block rank, z =
+    // group (one group of all heads is the plain order).  Packed batch:
+    // head-major, x = block rank, y / z = (sequence, query head).  Either way
+    // the CTAs that re-read the same K / V run close together.
+    const int bh = VARLEN ? grid_block() : static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
+    const int rank = VARLEN ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
     if (rank >= args.num_qblocks || (VARLEN && bh >= args.BH)) return;   // padding CTA
     int qb = args.num_qblocks - 1 - rank;                          // heavy blocks first
     // TMA coordinates: the rows of this sequence start at tok0, the head
@@ -117,7 +117,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int r0 = q0 + kTile * t;
         nkv[t] = (r0 >= N) ? 0 : (CAUSAL ? min(nkv_all, r0 / kTile + 1) : nkv_all);
     }
-    const int n_iter = max(nkv[0], nkv[1]);
+    int n_iter = max(nkv[0], nkv[1]);
+
+    // Block-sparse layout: the key blocks the CTA visits are those that either
+    // of its two query tiles keeps (within its causal range), in order.  Entry
+    // = key block | 1 << 14 if tile 0 keeps it | 1 << 15 if tile 1 does; a tile
+    // that drops a listed block gives it P = 0.  Built by warp 3 before the
+    // roles start.
+    const uint16_t* blist = reinterpret_cast<const uint16_t*>(smem + C::LIST_OFF);
+    if (SPARSE && warp == 3) {
+        const uint8_t* mrow0 = args.block_mask + bh * args.mask_head_stride +
+                               static_cast<long long>(q0 / kTile) * args.mask_cols;
+        uint16_t* wl = reinterpret_cast<uint16_t*>(smem + C::LIST_OFF);
+        int n = 0;
+        for (int c0 = 0; c0 < n_iter; c0 += 32) {
+            const int kb = c0 + lane;
+            const bool a0 = kb < nkv[0] && mrow0[kb] != 0;
+            const bool a1 = kb < nkv[1] && mrow0[args.mask_cols + kb] != 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, a0 || a1);
+            if (a0 || a1)
+                wl[n + __popc(bal & ((1u << lane) - 1u))] =
+                    static_cast<uint16_t>(kb | (a0 ? 1 << 14 : 0) | (a1 ? 1 << 15 : 0));
+            n += __popc(bal);
+        }
+        if (lane == 0) *reinterpret_cast<int*>(smem + C::MISC_OFF + 8) = n;
+    }
+    auto kblk = [&](int j) -> int { return SPARSE ? (blist[j] & 0x3FFF) : j; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
@@ -155,7 +180,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, args.status, args.wait_polls};
-    const bool skip = *abort_flag != 0;
+    bool skip = *abort_flag != 0;
+    if constexpr (SPARSE) {
+        n_iter = *reinterpret_cast<const int*>(smem + C::MISC_OFF + 8);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) nkv[t] = nkv[t] > 0 ? n_iter : 0;
+        if (n_iter == 0 && !skip) {
+            // every tile of these rows is dropped: empty softmax, O = 0, lse = -inf
+            const int rows = min(C::TILES * kTile, N - q0);
+            const size_t base = (static_cast<size_t>(bh) * N + q0) * D;
+            for (int e = threadIdx.x; e < rows * (D / 8); e += C::THREADS)
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + base)[e] = make_uint4(0u, 0u, 0u, 0u);
+            if (TRAIN)
+                for (int e = threadIdx.x; e < rows * (D / 4); e += C::THREADS)
+                    reinterpret_cast<float4*>(args.o32 + base)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = threadIdx.x; e < rows; e += C::THREADS)
+                args.lse[static_cast<size_t>(bh) * N + q0 + e] = -INFINITY;
+        }
+        if (n_iter == 0) skip = true;
+    }
 
     if (warp < 4) {
         if (skip) {
@@ -182,11 +225,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                    bar(C::B_KFULL + s), b * kBoxCols, tok0 + j * kTile, hk, pol_kv);
+                                    bar(C::B_KFULL + s), b * kBoxCols, tok0 + kblk(j) * kTile, hk, pol_kv);
                     mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                    bar(C::B_VFULL + s), b * kBoxCols, tok0 + j * kTile, hk, pol_kv);
+                                    bar(C::B_VFULL + s), b * kBoxCols, tok0 + kblk(j) * kTile, hk, pol_kv);
                     issued = j + 1;
                 }
                 if (!ok) {
@@ -282,11 +325,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL + t), j & 1));
                 if (!ok) break;
                 tc_fence_after();
+                if constexpr (SPARSE) {
+                    if (((blist[j] >> (14 + t)) & 1) == 0) {
+                        // this tile drops the block: P = 0, row state unchanged
+                        uint32_t zz[32];
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) zz[e] = 0u;
+                        tmem_st32(s_addr, zz);
+                        tmem_st32(s_addr + 32, zz);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(bar(C::B_PFULL + t));
+                        continue;
+                    }
+                }
                 float sv[128];
                 tmem_ld_sync(s_addr, sv);
                 // mask: key tail (keys >= N) and, on the diagonal block, keys > row
-                int limit = N - j * kTile;
-                if (CAUSAL) limit = min(limit, row - j * kTile + 1);
+                const int kb = kblk(j);
+                int limit = N - kb * kTile;
+                if (CAUSAL) limit = min(limit, row - kb * kTile + 1);
                 if (limit < kTile) {
     #pragma unroll
                     for (int c = 0; c < kTile; ++c)
@@ -374,7 +432,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // multiplied V, so each fp32 output row is a convex combination of V
                 // rows (weights summing to 1) and rowsum(dO o O) matches the P the
                 // backward recomputes; lse keeps the exact sum either way.
-                const float inv_l = 1.0f / (TRAIN ? lb : l);
+                const float den = TRAIN ? lb : l;
+                // (block-sparse: a row whose kept tiles were all above the
+                // diagonal has an empty softmax, O = 0)
+                const float inv_l = (SPARSE && !(den > 0.f)) ? 0.f : 1.0f / den;
                 const bool issuer = (warp & 3) == 0 && lane == 0;
                 const uint32_t stage = sbase + C::Q_OFF + t * C::TILE_BYTES;
                 uint8_t* stage_row = smem + C::Q_OFF + t * C::TILE_BYTES + r * 128;
@@ -473,7 +534,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // kernel, and waiting for them here kept the next CTA off the SM.
                 if (row < N)
                     args.lse[static_cast<size_t>(bh) * (VARLEN ? args.max_seqlen : N) + row] =
-                        (m_ref + __log2f(l)) * kLn2;
+                        ((SPARSE && !(l > 0.f)) ? -INFINITY : (m_ref + __log2f(l)) * kLn2);
             }
         }
     }
@@ -486,20 +547,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE = false>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to,
                                 const CUtensorMap& to32, const FwdArgs& a, int BH,
                                 cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN, VARLEN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN, VARLEN, SPARSE>;
+    constexpr int smem = SPARSE ? C::SMEM_SPARSE : C::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid = VARLEN ? head_major_grid(a.num_qblocks, BH)
-                      : a.head_group > 0 ? group_grid(a.num_qblocks, BH, a.head_group)
-                                         : lpt_grid(a.num_qblocks, BH);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, to32, a);
+                             : group_grid(a.num_qblocks, BH, a.head_group > 0 ? a.head_group : BH);
+    kern<<<grid, C::THREADS, smem, stream>>>(tq, tk, tv, to, to32, a);
     return cudaGetLastError();
 }
 
@@ -507,8 +567,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
                        int d, bool causal, bool bf16, cudaStream_t stream) {
     const bool varlen = a.cu_seqlens != nullptr;
+    const bool sparse = a.block_mask != nullptr;
 #define ATTN_FWD_CASE(D_, C_, B_)                                                                   \
     if (d == D_ && causal == C_ && bf16 == B_) {                                                    \
+        if (sparse)                                                                                 \
+            return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true, false, true>(tq, tk, tv, to, to32, a, BH, stream) \
+                                    : launch_fwd_t<D_, C_, B_, false, false, true>(tq, tk, tv, to, to32, a, BH, stream); \
         if (varlen)                                                                                 \
             return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true, true>(tq, tk, tv, to, to32, a, BH, stream) \
                                     : launch_fwd_t<D_, C_, B_, false, true>(tq, tk, tv, to, to32, a, BH, stream); \

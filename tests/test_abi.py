@@ -68,6 +68,7 @@ def test_forward_argument_errors(L):
     assert _fwd(L, B=0) == 1
     assert _fwd(L, N=0) == 1
     assert _fwd(L, N=(1 << 24) + 1) == 1
+    assert _fwd(L, N=(1 << 24) - 255) == 1     # one 256-row block past the grid limit
     assert _fwd(L, d=32) == 2
     assert _fwd(L, d=96) == 2
     assert _fwd(L, d=256) == 2
@@ -174,3 +175,38 @@ def test_grouped_entry_point_argument_errors(L):
     assert L.attn_bwd_preprocess_gqa(A, A, A, A, A, A, A, 1, 6, 4, 128, 64, 1, 0.125, None) == 1
     assert L.attn_bwd_gqa(A, A, A, A, A, A, A, A, A, A, 1, 6, 4, 128, 64, 1, 0.125, None) == 1
     assert L.attn_bwd_gqa(A, A, A, A, A, A, A, A, A, A, 1, 6, 3, 128, 80, 1, 0.125, None) == 2
+
+
+def test_block_sparse_argument_errors(L):
+    """Mask arguments are checked on the host before anything is enqueued."""
+    def fwd(mask=A, stride=0, N=1000, o32=None, **kw):
+        a = dict(B=1, H=2, d=64, causal=1, scale=0.125)
+        a.update(kw)
+        if o32 is None:
+            return L.attn_fwd_bsparse(A, A, A, A, A, mask, stride, a["B"], a["H"], N, a["d"],
+                                      a["causal"], a["scale"], None)
+        return L.attn_fwd_train_bsparse(A, A, A, A, o32, A, mask, stride, a["B"], a["H"], N,
+                                        a["d"], a["causal"], a["scale"], None)
+
+    def bwd(mask=A, stride=0, N=1000):
+        return L.attn_bwd_bsparse(A, A, A, A, A, A, A, A, A, A, mask, stride, 1, 2, N, 64, 1,
+                                  0.125, None)
+
+    nb = (1000 + 127) // 128
+    assert fwd() in (0, 4)                       # valid: no device here
+    assert fwd(stride=nb * nb) in (0, 4)
+    assert fwd(mask=None) == 1
+    assert fwd(stride=-1) == 1
+    assert fwd(stride=nb * nb - 1) == 1          # per-head masks would overlap
+    assert fwd(N=384 * 128) in (0, 4)
+    assert fwd(N=384 * 128 + 1) == 1             # beyond the shared-memory tile list
+    assert fwd(d=96) == 2
+    assert fwd(o32=None, scale=0.0) == 1
+    assert fwd(o32=0) == 1                       # the training variant needs o32
+    assert fwd(o32=A + 4) == 3
+    assert bwd() in (0, 4)
+    assert bwd(mask=None) == 1
+    assert bwd(stride=5) == 1
+    assert bwd(N=50000) == 1
+    assert L.attn_bwd_bsparse_f16(A, A, A, A, A, A, A, A, A, None, A, 0, 1, 2, 1000, 64, 1,
+                                  0.125, None) == 1
