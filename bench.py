@@ -511,6 +511,93 @@ def run_varlen(args):
     }))
 
 
+def run_bsparse(args):
+    """The training step (forward with fp32 O, D preprocess, backward) with a
+    block-sparse layout on the causal B=2 H=16 N=8192 d=128 shape (Q and K
+    x3): a seeded random mask per head keeping each 128 x 128 tile with
+    probability --bsparse, the diagonal tiles always kept.  FLOPs count only
+    the (query, key) pairs the kept tiles leave visible, 10 d per pair (the
+    dense causal step is 10 B H N^2 d / 2 in the same convention); the dense
+    step on the same inputs is timed beside it."""
+    import torch
+    import numpy as np
+    import io_aware_exact_gb300 as attn
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[HEADLINE]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    nb = (N + 127) // 128
+    rng = np.random.default_rng(4321)
+    mask = (rng.random((B, H, nb, nb)) < args.bsparse).astype(np.uint8)
+    mask[:, :, np.arange(nb), np.arange(nb)] = 1
+    rows = np.minimum(128, N - 128 * np.arange(nb))
+    full = np.outer(rows, rows).astype(np.float64)
+    vis = np.tril(full, -1) + np.diag(rows * (rows + 1) / 2.0)      # causal visible pairs
+    pairs = float((mask * vis[None, None]).sum())
+    flops = 10.0 * d * pairs
+    kept = float((mask * (vis > 0)[None, None]).sum() / ((vis > 0).sum() * B * H))
+    x = {n: t.to(dev) for n, t in make_inputs(B, H, N, d, seed=w.seed, qk_mult=w.qk_mult).items()}
+    q, k, v, dO = x["q"], x["k"], x["v"], x["dO"]
+    m = torch.from_numpy(mask).to(dev)
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def sparse_step(mid):
+        attn.forward_bsparse(q, k, v, m, True, scale, o=o, lse=lse, o32=o32, stream=stream)
+        mid.record(stream)
+        attn.backward_bsparse(q, k, v, o32, lse, dO, m, True, scale, dq=dq, dk=dk, dv=dv, D=D,
+                              dq_accum=acc, stream=stream)
+
+    def dense_step(mid):
+        attn.forward(q, k, v, True, scale, o=o, lse=lse, o32=o32, stream=stream)
+        mid.record(stream)
+        attn.backward(q, k, v, None, lse, dO, True, scale, dq=dq, dk=dk, dv=dv, D=D,
+                      dq_accum=acc, stream=stream, o32=o32)
+
+    def timed(step):
+        for _ in range(args.warmup):
+            step(torch.cuda.Event())
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step(evs[i][2])
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        if attn.attn_get_device_status() != 0:
+            raise RuntimeError("device status set during the block-sparse steps")
+        return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                statistics.mean(e[0].elapsed_time(e[2]) for e in evs))
+
+    with ClockSampler(0) as clk:
+        ms, ms_fwd = timed(sparse_step)
+        ms_dense, _ = timed(dense_step)
+    peak = _peaks().get("bf16_tflops_sustained")
+    value = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "attention TFLOPS fwd+bwd, block-sparse layout (kept pairs only)",
+        "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), Q and K x3)",
+        "config": {"workload": "bsparse_causal_b2_h16_n8192_d128", "B": B, "H": H, "N": N, "d": d,
+                   "causal": True, "tile": 128, "keep_probability": args.bsparse,
+                   "kept_tile_fraction": round(kept, 4), "mask": "seeded random per head, diagonal kept",
+                   "l2": "L2 flushed (512 MB write) between steps"},
+        "frac_of_peak": round(value / peak, 4) if peak else None,
+        "fwd_train_ms": round(ms_fwd, 4), "bwd_ms": round(ms - ms_fwd, 4),
+        "dense_step_ms": round(ms_dense, 4), "speedup_vs_dense": round(ms_dense / ms, 3),
+        "clocks": clk.summary(),
+    }))
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, timed on the host cores.
 
@@ -578,11 +665,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--varlen", action="store_true",
                     help="time the step on a packed variable-length batch instead")
+    ap.add_argument("--bsparse", type=float, default=0.0,
+                    help="time the step with a random block-sparse layout keeping this "
+                         "fraction of tiles instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.varlen:
         run_varlen(args)
+    elif args.bsparse > 0:
+        run_bsparse(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
