@@ -340,3 +340,47 @@ def attention_backward_block_sparse(q, k, v, dO, block_mask, causal: bool, scale
     """(dQ, dK, dV, lse, D) of one head under a block-sparse layout."""
     vis = expand_block_mask(block_mask, len(q), len(k), block, causal)
     return attention_backward_masked(q, k, v, dO, vis, scale)
+
+
+def merge_partials(o1, lse1, o2, lse2):
+    """Exact merge of two partial results of the same query rows over
+    disjoint key sets (sj-techlog "FlashAttention 원 논문 해부", section "두
+    tile을 한 row로 합치는 식": both states are rescaled by exp of their
+    statistic minus the new maximum and the normaliser is renormalised).
+    With normalised outputs o and natural-log logsumexps lse:
+    lse = m + ln(e^{lse1-m} + e^{lse2-m}), m = max(lse1, lse2), and
+    o = e^{lse1-lse} o1 + e^{lse2-lse} o2.  A side with lse = -inf (no
+    visible key) has weight 0; two such sides give o = 0, lse = -inf."""
+    o1, o2 = _f64(o1), _f64(o2)
+    lse1, lse2 = _f64(lse1), _f64(lse2)
+    m = np.maximum(lse1, lse2)
+    fin = np.isfinite(m)
+    ms = np.where(fin, m, 0.0)
+    e1 = np.where(fin, np.exp(lse1 - ms), 0.0)
+    e2 = np.where(fin, np.exp(lse2 - ms), 0.0)
+    z = np.where(fin, e1 + e2, 1.0)
+    lse = np.where(fin, ms + np.log(z), -np.inf)
+    w1, w2 = e1 / z, e2 / z
+    return w1[..., None] * o1 + w2[..., None] * o2, lse
+
+
+def attention_backward_given_stats(q, k, v, dO, lse, D, causal: bool, scale: float,
+                                   q_offset: int = 0):
+    """(dQ, dK, dV) of one head's queries against one key / value chunk, with
+    the rows' logsumexp and D taken as given (those of the whole key set the
+    rows attend to): P_ij = exp(tau q_i.k_j - lse_i) on visible pairs, then
+    the FlashAttention-2 review's backward ("Backward Pass"): dV = P^T dO,
+    dP = dO V^T, dS = P o (dP - D), dQ = tau dS K, dK = tau dS^T Q.  Summed
+    over the chunks of a split key set these are the gradients of the whole.
+    With ``causal`` query i (row i + q_offset of the sequence, keys numbered
+    from 0 in this chunk) sees key j iff j <= i + q_offset."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    lse, D = _f64(lse), _f64(D)
+    nq, nk = len(q), len(k)
+    vis = np.ones((nq, nk), bool)
+    if causal:
+        vis = np.arange(nk)[None, :] <= (np.arange(nq)[:, None] + q_offset)
+    p = np.where(vis, np.exp(np.where(vis, scale * (q @ k.T), 0.0) - lse[:, None]), 0.0)
+    dp = dO @ v.T
+    ds = p * (dp - D[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), p.T @ dO

@@ -504,3 +504,72 @@ def test_block_sparse_backward_matches_finite_differences():
         scale = max(1.0, np.max(np.abs(want)))
         assert np.max(np.abs(got - want)) / scale < 1e-6
     assert np.all(dq[3:6] == 0.0) and np.all(D[3:6] == 0.0)
+
+
+# --------------------------------------------------------------------------
+# Combining partial results over a split key set
+# --------------------------------------------------------------------------
+
+def test_merge_partials_reproduces_printed_merge_example():
+    """sj-techlog page, section "12살 숫자 예": the state m = 2, l = 1.5, u = 6
+    merged with the new tile (scores [3, 1], values [10, 20]; printed
+    tilde_l, tilde_u) gives the printed l', o'."""
+    g = _golden("page1_merge_example.json")
+    st, pr, rnd = g["state_before"], g["printed"], g["printed_rounding"]
+    o1, lse1 = st["u"] / st["l"], st["m"] + math.log(st["l"])
+    o2, lse2 = pr["tilde_u"] / pr["tilde_l"], pr["m_new"] + math.log(pr["tilde_l"])
+    o, lse = oracle.merge_partials([[o1]], [lse1], [[o2]], [lse2])
+    assert abs(o[0, 0] - pr["o_new"]) <= rnd["o_new"]
+    assert abs(math.exp(lse[0] - pr["m_new"]) - pr["l_new"]) <= rnd["l_new"]
+
+
+@pytest.mark.parametrize("split", [1, 3, 6])
+def test_merge_of_key_chunks_is_full_attention(split):
+    """Attention over keys [0, split) and [split, n) separately (C oracle),
+    merged, equals attention over all keys; merging with an empty partial
+    (lse = -inf) changes nothing."""
+    r = _rng(90 + split)
+    n, tau = 7, 0.9
+    q, k, v = r.normal(size=(5, 3)), r.normal(size=(n, 3)), r.normal(size=(n, 2))
+    o1, l1 = oracle.attention_forward(q, k[:split], v[:split], False, tau)
+    o2, l2 = oracle.attention_forward(q, k[split:], v[split:], False, tau)
+    o, lse = oracle.merge_partials(o1, l1, o2, l2)
+    of, lf = oracle.attention_forward(q, k, v, False, tau)
+    assert np.max(np.abs(o - of)) < 1e-13 and np.max(np.abs(lse - lf)) < 1e-13
+    oe, le = oracle.merge_partials(o, lse, np.full_like(o, 7.0), np.full(len(o), -np.inf))
+    assert np.array_equal(oe, o) and np.array_equal(le, lse)
+    oz, lz = oracle.merge_partials(np.ones((2, 2)), [-np.inf] * 2, np.ones((2, 2)), [-np.inf] * 2)
+    assert np.all(oz == 0.0) and np.all(np.isneginf(lz))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_given_stats_sums_to_full_backward(causal):
+    """Gradients of one query chunk against each key chunk, with the whole
+    row's lse and D given, sum to the full backward (C oracle): dQ is the sum
+    over key chunks and dK, dV of a key chunk are its rows of the full
+    result.  With the chunk's own statistics it is the plain backward."""
+    r = _rng(95 + int(causal))
+    n, nc, tau = 8, 4, 0.7
+    q, k = r.normal(size=(n, 3)), r.normal(size=(n, 3))
+    v, dO = r.normal(size=(n, 2)), r.normal(size=(n, 2))
+    dq, dk, dv, lse, D = oracle.attention_backward(q, k, v, dO, causal, tau)
+    for qc in range(0, n, nc):
+        rows = slice(qc, qc + nc)
+        dq_sum = np.zeros((nc, 3))
+        for kc in range(0, n, nc):
+            if causal and kc > qc:
+                continue
+            cols = slice(kc, kc + nc)
+            gq, _, _ = oracle.attention_backward_given_stats(
+                q[rows], k[cols], v[cols], dO[rows], lse[rows], D[rows], causal, tau,
+                q_offset=qc - kc)
+            dq_sum += gq
+            # all query rows against this key chunk give its rows of dK, dV
+            full_k = oracle.attention_backward_given_stats(q, k[cols], v[cols], dO, lse, D,
+                                                           causal, tau, q_offset=-kc)
+            assert np.max(np.abs(full_k[1] - dk[cols])) < 1e-12
+            assert np.max(np.abs(full_k[2] - dv[cols])) < 1e-12
+        assert np.max(np.abs(dq_sum - dq[rows])) < 1e-12
+    own = oracle.attention_backward_given_stats(q, k, v, dO, lse, D, causal, tau)
+    for a, b in zip(own, (dq, dk, dv)):
+        assert np.max(np.abs(a - b)) < 1e-12
