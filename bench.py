@@ -598,6 +598,71 @@ def run_bsparse(args):
     }))
 
 
+def run_ring(args):
+    """Ring attention emulated on one GPU: the causal B=2 H=16 N=8192 d=128
+    training step (Q and K x3) with the sequence split into --ring chunks,
+    every (query chunk, key chunk) pair run by the library's kernels and the
+    partial results merged (attn_merge) and accumulated (attn_accumulate) as
+    a ring of that many devices would.  FLOPs as for the dense causal step;
+    the dense step on the same inputs is timed beside it, so the difference
+    is what splitting into chunks costs on one device."""
+    import torch
+    import io_aware_exact_gb300 as attn
+    from io_aware_exact_gb300 import ring
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[HEADLINE]
+    B, H, N, d, R = w.B, w.H, w.N, w.d, args.ring
+    if N % R or (N // R) % 8:
+        raise SystemExit("--ring must split N into equal chunks")
+    x = {n: t.to(dev) for n, t in make_inputs(B, H, N, d, seed=w.seed, qk_mult=w.qk_mult).items()}
+    ch = {n: [c.contiguous() for c in torch.chunk(t, R, dim=2)] for n, t in x.items()}
+    scale = d ** -0.5
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def ring_step():
+        o, lse, o32 = ring.ring_forward(ch["q"], ch["k"], ch["v"], True, scale)
+        ring.ring_backward(ch["q"], ch["k"], ch["v"], o32, lse, ch["dO"], True, scale)
+
+    def dense_step():
+        o, lse, o32 = attn.forward(x["q"], x["k"], x["v"], True, scale, o32=True)
+        attn.backward(x["q"], x["k"], x["v"], None, lse, x["dO"], True, scale, o32=o32)
+
+    def timed(step):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        if attn.attn_get_device_status() != 0:
+            raise RuntimeError("device status set during the ring steps")
+        return statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+
+    with ClockSampler(0) as clk:
+        ms = timed(ring_step)
+        ms_dense = timed(dense_step)
+    flops = 10.0 * B * H * N * N * d / 2
+    peak = _peaks().get("bf16_tflops_sustained")
+    value = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "attention TFLOPS fwd+bwd, ring attention emulated on one GPU",
+        "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), Q and K x3)",
+        "config": {"workload": "ring_causal_b2_h16_n8192_d128", "chunks": R, "chunk_len": N // R,
+                   "l2": "L2 flushed (512 MB write) between steps"},
+        "frac_of_peak": round(value / peak, 4) if peak else None,
+        "dense_step_ms": round(ms_dense, 4), "ring_over_dense": round(ms / ms_dense, 3),
+        "clocks": clk.summary(),
+    }))
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, timed on the host cores.
 
@@ -665,6 +730,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--varlen", action="store_true",
                     help="time the step on a packed variable-length batch instead")
+    ap.add_argument("--ring", type=int, default=0,
+                    help="time the step as ring attention over this many chunks, emulated "
+                         "on one GPU, instead")
     ap.add_argument("--bsparse", type=float, default=0.0,
                     help="time the step with a random block-sparse layout keeping this "
                          "fraction of tiles instead")
@@ -675,6 +743,8 @@ def main():
         run_varlen(args)
     elif args.bsparse > 0:
         run_bsparse(args)
+    elif args.ring > 0:
+        run_ring(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -306,6 +306,64 @@ int attn_bwd_bsparse_f16(const void* q, const void* k, const void* v, const void
                          void* dv, const void* block_mask, long long mask_head_stride, int B,
                          int H, int N, int d, int causal, float scale, void* stream);
 
+/*
+ * Combining partial results: the building blocks of attention over a
+ * sequence whose keys and values are split into chunks (ring attention: the
+ * paldyn.com survey "어텐션 비용 줄이기", section "다중 GPU 확장", has each
+ * device keep its share of Q and pass K / V blocks around a ring, running the
+ * single-device kernel on each pair).
+ *
+ * attn_merge merges a partial forward result into a running one, row by row,
+ * in place: o_acc, o_part are [rows, d] fp32 outputs each normalised over its
+ * own keys (the o32 of attn_fwd_train), lse_acc, lse_part [rows] their
+ * natural-log logsumexps.  The merge is exact (sj-techlog "FlashAttention 원
+ * 논문 해부", section "두 tile을 한 row로 합치는 식", written with normalised
+ * outputs):
+ *   L = log(exp(L_acc) + exp(L_part)),
+ *   O = exp(L_acc - L) O_acc + exp(L_part - L) O_part,
+ * with the larger statistic subtracted first; a side with L = -inf has
+ * weight 0 and two of them give O = 0, L = -inf.  If o_out is not NULL the
+ * merged O is also written there rounded to 16 bits ([rows, d]; bfloat16, or
+ * IEEE half for the _f16 twin).  d is 64 or 128; o_acc, o_part, o_out
+ * 16-byte aligned.  For [B,H,N,d] tensors rows = B*H*N.
+ *
+ * attn_convert writes y = scale * x rounded to 16 bits (the final cast of an
+ * fp32 result such as a gradient summed over chunks).  elems must be a
+ * multiple of 8; pointers 16-byte aligned.
+ *
+ * Both are element-wise passes over device memory; argument errors
+ * return ATTN_ERR_INVALID_ARG (or _MISALIGNED / _UNSUPPORTED_HEAD_DIM) with
+ * nothing enqueued, rows = 0 / elems = 0 enqueue nothing.
+ */
+int attn_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+               void* o_out, long long rows, int d, void* stream);
+int attn_merge_f16(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                   void* o_out, long long rows, int d, void* stream);
+int attn_convert(const float* x, void* y, long long elems, float scale, void* stream);
+int attn_convert_f16(const float* x, void* y, long long elems, float scale, void* stream);
+
+/*
+ * Backward pass against one key / value chunk with fp32 dK, dV: as attn_bwd
+ * (grouped heads allowed, Hkv as for attn_bwd_gqa), but instead of 16-bit dk,
+ * dv it writes dk32, dv32 [B,Hkv,N,d] fp32, or adds to them when accumulate
+ * is nonzero.  With lse and D of the whole rows (from the merged forward and
+ * attn_bwd_preprocess_o32 of the merged fp32 O), the backward of a query
+ * chunk against each key chunk yields that pair's share of the gradients
+ * (the FlashAttention-2 review's "Backward Pass" with P = exp(S - lse)), so
+ * the shares of dK, dV summed here over the query chunks, and of dQ summed in
+ * dq_accum, are the gradients of the whole sequence, with no 16-bit rounding
+ * of the partial sums.  dq is written from dq_accum after each call.
+ * Dense layout only; dk32, dv32 16-byte aligned.
+ */
+int attn_bwd_acc(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                 const float* D, float* dq_accum, void* dq, float* dk32, float* dv32,
+                 int accumulate, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 void* stream);
+int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, float* dk32,
+                     float* dv32, int accumulate, int B, int H, int Hkv, int N, int d,
+                     int causal, float scale, void* stream);
+
 /* Static English description of a status code. */
 const char* attn_status_string(int status);
 

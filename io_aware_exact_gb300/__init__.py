@@ -99,6 +99,19 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = at
                 fn.restype = I
+            # combining partial results
+            for name in ("attn_merge", "attn_merge_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, P, P, LL, I, P]
+                fn.restype = I
+            for name in ("attn_bwd_acc", "attn_bwd_acc_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+                fn.restype = I
+            for name in ("attn_convert", "attn_convert_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, LL, F, P]
+                fn.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -352,6 +365,44 @@ def backward_bsparse(q, k, v, o32, lse, dO, block_mask, causal: bool = False, sc
                      D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                      dv.data_ptr(), mp, ms, B, H, N, d, causal, scale, s, f16)
     return dq, dk, dv
+
+
+def merge(o_acc, lse_acc, o_part, lse_part, o_out=None, stream=None):
+    """Merge a partial result (fp32 O [..., d] normalised over its keys, lse
+    [...]) into a running one, in place; optionally also write the merged O
+    rounded to o_out's 16-bit dtype."""
+    torch = _torch()
+    d = o_acc.shape[-1]
+    rows = lse_acc.numel()
+    for t in (o_acc, lse_acc, o_part, lse_part):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("merge takes contiguous fp32 CUDA tensors")
+    if o_part.shape != o_acc.shape or lse_part.numel() != rows or o_acc.numel() != rows * d:
+        raise ValueError("merge: shapes of the two partial results differ")
+    f16 = o_out is not None and o_out.dtype == torch.float16
+    fn = lib().attn_merge_f16 if f16 else lib().attn_merge
+    _check(fn(o_acc.data_ptr(), lse_acc.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+              None if o_out is None else o_out.data_ptr(), rows, d, _stream_handle(stream)),
+           "attn_merge")
+
+
+def attn_bwd_acc(q, k, v, dO, lse, D, dq_accum, dq, dk32, dv32, accumulate, B, H, Hkv, N, d,
+                 causal, scale, stream, f16=False):
+    """Backward against one key / value chunk writing (or, with accumulate,
+    adding to) fp32 dK, dV."""
+    fn = lib().attn_bwd_acc_f16 if f16 else lib().attn_bwd_acc
+    _check(fn(q, k, v, dO, lse, D, dq_accum, dq, dk32, dv32, int(bool(accumulate)), B, H, Hkv, N,
+              d, int(bool(causal)), float(scale), stream), "attn_bwd_acc")
+
+
+def convert(x, dtype, scale: float = 1.0, out=None, stream=None):
+    """scale * x (fp32) rounded to a 16-bit dtype."""
+    torch = _torch()
+    out = torch.empty(x.shape, dtype=dtype, device=x.device) if out is None else out
+    fn = lib().attn_convert_f16 if out.dtype == torch.float16 else lib().attn_convert
+    _check(fn(x.data_ptr(), out.data_ptr(), x.numel(), float(scale), _stream_handle(stream)),
+           "attn_convert")
+    return out
 
 
 def _autograd_function():

@@ -261,7 +261,13 @@ int pre_o32_impl(const float* o32, const void* dO, float* D, float* dq_accum, in
 int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
              const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int Hkv,
              int N, int d, int causal, float scale, void* stream, bool bf16,
-             const void* block_mask = nullptr, long long mask_stride = 0) {
+             const void* block_mask = nullptr, long long mask_stride = 0,
+             float* dk32 = nullptr, float* dv32 = nullptr, int acc32 = 0) {
+    // with fp32 gradient outputs (dk32, dv32) the 16-bit dk, dv are not used
+    const bool f32 = dk32 != nullptr || dv32 != nullptr;
+    if (f32 && (!dk32 || !dv32)) return ATTN_ERR_INVALID_ARG;
+    if (f32 && !aligned16(dv32)) return ATTN_ERR_MISALIGNED;
+    if (f32) dk = dv = dk32;
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
@@ -281,9 +287,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
         (rc = make_map(&tv, v, BHkv, N, d, bf16)) || (rc = make_map(&tdo, dO, BH, N, d, bf16)))
         return rc;
     CUtensorMap tdq, tdk, tdv;
-    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d)) || (rc = make_map(&tdk, dk, BHkv, N, d, bf16)) ||
-        (rc = make_map(&tdv, dv, BHkv, N, d, bf16)))
+    if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d))) return rc;
+    if (f32) {
+        tdk = tdv = tq;   // not used: the fp32 rows are written directly
+    } else if ((rc = make_map(&tdk, dk, BHkv, N, d, bf16)) || (rc = make_map(&tdv, dv, BHkv, N, d, bf16))) {
         return rc;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     BwdArgs a{};
     a.lse = lse;
@@ -303,6 +312,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.block_mask = static_cast<const uint8_t*>(block_mask);
     a.mask_head_stride = mask_stride;
     a.mask_cols = a.num_kvblocks;
+    a.dk32 = dk32;
+    a.dv32 = dv32;
+    a.acc32 = acc32;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -488,6 +500,35 @@ __global__ void selftest_timeout_kernel(int* status, unsigned int max_polls) {
     // Nothing ever arrives on the barrier: the wait must run out and report.
     const WaitCtx wc{&abort_flag, status, max_polls};
     if (threadIdx.x == 0) (void)wait_bar(wc, b, 0);
+}
+
+int merge_impl(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+               void* o_out, long long rows, int d, void* stream, bool bf16) {
+    if (!o_acc || !lse_acc || !o_part || !lse_part || rows < 0) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!aligned16(o_acc) || !aligned16(o_part) || (o_out && !aligned16(o_out)))
+        return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    int rc = current_device(&status);
+    if (rc) return rc;
+    if (rows == 0) return ATTN_OK;
+    MergeArgs a{o_acc, lse_acc, o_part, lse_part, o_out, rows, d};
+    return map_launch(launch_merge(a, bf16, static_cast<cudaStream_t>(stream)));
+}
+
+int convert_impl(const float* x, void* y, long long elems, float scale, void* stream, bool bf16) {
+    if (!x || !y || elems < 0 || elems % 8 != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return ATTN_ERR_MISALIGNED;
+    int* status = nullptr;
+    int rc = current_device(&status);
+    if (rc) return rc;
+    if (elems == 0) return ATTN_OK;
+    DqConvertArgs c{};
+    c.dq_accum = x;
+    c.dq = y;
+    c.elems = elems;
+    c.scale = scale;
+    return map_launch(launch_dq_convert(c, bf16, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -759,5 +800,41 @@ int attn_selftest_timeout(int timeout_us, void* stream) {
 }
 
 const char* attn_version(void) { return "io_aware_exact_gb300 0.1 (sm_103a)"; }
+
+int attn_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+               void* o_out, long long rows, int d, void* stream) {
+    return attn::merge_impl(o_acc, lse_acc, o_part, lse_part, o_out, rows, d, stream, true);
+}
+
+int attn_merge_f16(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                   void* o_out, long long rows, int d, void* stream) {
+    return attn::merge_impl(o_acc, lse_acc, o_part, lse_part, o_out, rows, d, stream, false);
+}
+
+int attn_bwd_acc(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                 const float* D, float* dq_accum, void* dq, float* dk32, float* dv32,
+                 int accumulate, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 void* stream) {
+    if (!dk32 || !dv32) return ATTN_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, nullptr, nullptr, B, H, Hkv, N, d, causal,
+                    scale, stream, true, nullptr, 0, dk32, dv32, accumulate != 0);
+}
+
+int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, float* dk32,
+                     float* dv32, int accumulate, int B, int H, int Hkv, int N, int d,
+                     int causal, float scale, void* stream) {
+    if (!dk32 || !dv32) return ATTN_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, nullptr, nullptr, B, H, Hkv, N, d, causal,
+                    scale, stream, false, nullptr, 0, dk32, dv32, accumulate != 0);
+}
+
+int attn_convert(const float* x, void* y, long long elems, float scale, void* stream) {
+    return attn::convert_impl(x, y, elems, scale, stream, true);
+}
+
+int attn_convert_f16(const float* x, void* y, long long elems, float scale, void* stream) {
+    return attn::convert_impl(x, y, elems, scale, stream, false);
+}
 
 }  // extern "C"

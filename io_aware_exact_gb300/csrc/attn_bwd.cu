@@ -929,12 +929,33 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // also cover the first rows of the next sequence, so each thread
                     // stores its own key row (rows past the sequence are not written).
                     const bool direct = varlen && (j + 1) * kTile > N;
+                    // fp32 output (written, or added to a running sum, row by row)
+                    const bool f32out = GENERAL && args.dk32 != nullptr;
                     uint16_t* drow = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
                                      (static_cast<size_t>(tok0 + j * kTile + r) * args.Hkv + kvc) * D;
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
                         tmem_ld_sync(tmem + lane_off + col + cc, a32);
+                        if (f32out) {
+                            if (key_ok) {
+                                float* frow = (c == 0 ? args.dv32 : args.dk32) +
+                                              (static_cast<size_t>(kvc) * N + j * kTile + r) * D + cc;
+        #pragma unroll
+                                for (int v4 = 0; v4 < 8; ++v4) {
+                                    float4 o = make_float4(__uint_as_float(a32[4 * v4]) * mul,
+                                                           __uint_as_float(a32[4 * v4 + 1]) * mul,
+                                                           __uint_as_float(a32[4 * v4 + 2]) * mul,
+                                                           __uint_as_float(a32[4 * v4 + 3]) * mul);
+                                    if (args.acc32) {
+                                        const float4 p = *reinterpret_cast<const float4*>(frow + 4 * v4);
+                                        o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+                                    }
+                                    *reinterpret_cast<float4*>(frow + 4 * v4) = o;
+                                }
+                            }
+                            continue;
+                        }
                         uint32_t pk[16];
         #pragma unroll
                         for (int e = 0; e < 16; ++e)
@@ -956,7 +977,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
                                 make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
-                    if (direct) ok = false;   // stored; skip the TMA store below
+                    if (direct || f32out) ok = false;   // stored; skip the TMA store below
                     if (ok) {
                         fence_proxy_async_smem();
                         mbar_arrive(bar(C::B_EPI + c));
@@ -1065,7 +1086,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdv, const BwdArgs& a, int BH, int d, bool causal,
                        bool bf16, cudaStream_t stream) {
     // the dense MHA kernel's head-group grid holds at most 65,535 key blocks
-    const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr || a.num_kvblocks > kMaxGridY;
+    const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr || a.num_kvblocks > kMaxGridY ||
+                         a.dk32 != nullptr;
     const bool sparse = a.block_mask != nullptr;   // dense layout, Hkv = H only
     if (sparse && general) return cudaErrorInvalidValue;
 #define ATTN_BWD_CASE(D_, C_, B_)                                                              \

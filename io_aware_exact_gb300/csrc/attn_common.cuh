@@ -73,6 +73,11 @@ struct BwdArgs {
     const uint8_t* block_mask;
     long long mask_head_stride;
     int mask_cols;
+    // fp32 gradient outputs (dense layout, general kernel), nullptr: 16-bit dk, dv.
+    // dk32 / dv32 [B*Hkv, N, d] are overwritten, or added to when acc32 != 0.
+    float* dk32;
+    float* dv32;
+    int acc32;
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
@@ -107,6 +112,16 @@ struct DqConvertArgs {
     float scale;            // tau
 };
 
+struct MergeArgs {
+    float* o_acc;           // [rows, d] fp32 running output, merged in place
+    float* lse_acc;         // [rows] running logsumexp, merged in place
+    const float* o_part;    // [rows, d] fp32 partial output
+    const float* lse_part;  // [rows] partial logsumexp
+    void* o_out;            // [rows, d] 16-bit copy of the merged output, or nullptr
+    long long rows;
+    int d;
+};
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a, int BH,
@@ -120,6 +135,8 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
                             bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, bool bf16, cudaStream_t stream);
+
 
 // Grid layouts of the attention kernels.  Plain: x = (batch, head), y/z =
 // block index within a head.  Launch order is x fastest, so every head's

@@ -210,3 +210,30 @@ def test_block_sparse_argument_errors(L):
     assert bwd(N=50000) == 1
     assert L.attn_bwd_bsparse_f16(A, A, A, A, A, A, A, A, A, None, A, 0, 1, 2, 1000, 64, 1,
                                   0.125, None) == 1
+
+
+def test_combine_entry_points_argument_errors(L):
+    """attn_merge / attn_convert / attn_bwd_acc check their arguments on the host."""
+    assert L.attn_merge(A, A, A, A, None, 100, 128, None) in (0, 4)
+    assert L.attn_merge(A, A, A, A, A, 100, 64, None) in (0, 4)
+    assert L.attn_merge(None, A, A, A, None, 100, 128, None) == 1
+    assert L.attn_merge(A, A, A, None, None, 100, 128, None) == 1
+    assert L.attn_merge(A, A, A, A, None, -1, 128, None) == 1
+    assert L.attn_merge(A, A, A, A, None, 100, 96, None) == 2
+    assert L.attn_merge(A + 4, A, A, A, None, 100, 128, None) == 3
+    assert L.attn_merge_f16(A, A, A, A, A + 8, 100, 128, None) == 3
+    bwd = lambda **kw: L.attn_bwd_acc(*[kw.get(n, A) for n in ("q", "k", "v", "dO", "lse", "D",
+                                                                 "acc", "dq", "dk32", "dv32")],
+                                      kw.get("accumulate", 0), 1, 4, kw.get("Hkv", 2), 256, 128,
+                                      1, 0.1, None)
+    assert bwd() in (0, 4)
+    assert bwd(accumulate=1, Hkv=4) in (0, 4)
+    assert bwd(dk32=None) == 1
+    assert bwd(dv32=None) == 1
+    assert bwd(dv32=A + 4) == 3
+    assert bwd(Hkv=3) == 1                                 # H not a multiple of Hkv
+    assert bwd(dq=None) == 1
+    assert L.attn_convert(A, A, 64, 1.0, None) in (0, 4)
+    assert L.attn_convert(A, A, 12, 1.0, None) == 1       # not a multiple of 8
+    assert L.attn_convert(A, A, 64, float("nan"), None) == 1
+    assert L.attn_convert_f16(A, None, 64, 1.0, None) == 1
