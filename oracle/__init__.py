@@ -384,3 +384,96 @@ def attention_backward_given_stats(q, k, v, dO, lse, D, causal: bool, scale: flo
     dp = dO @ v.T
     ds = p * (dp - D[:, None])
     return scale * (ds @ k), scale * (ds.T @ q), p.T @ dO
+
+
+# --------------------------------------------------------------------------
+# Dropout (the sj-techlog page, backward section: the forward keeps the
+# pseudo-random generator's state and the backward regenerates the same
+# dropout mask from it instead of storing it).  The generator is Philox4x32-10
+# (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+# SC'11), written here from that definition.
+# --------------------------------------------------------------------------
+
+_PHILOX_M0, _PHILOX_M1 = 0xD2511F53, 0xCD9E8D57      # round multipliers
+_PHILOX_W0, _PHILOX_W1 = 0x9E3779B9, 0xBB67AE85      # Weyl key increments
+_MASK32 = 0xFFFFFFFF
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32 with 10 rounds.  counter: uint array [..., 4], key: uint
+    array [..., 2] (broadcast); returns uint32 [..., 4].  One round maps
+    (c0, c1, c2, c3) with key (k0, k1) to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2),
+    hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key gains (W0, W1) between rounds."""
+    c = [np.asarray(counter, dtype=np.uint64)[..., i] & _MASK32 for i in range(4)]
+    k0 = np.asarray(key, dtype=np.uint64)[..., 0] & _MASK32
+    k1 = np.asarray(key, dtype=np.uint64)[..., 1] & _MASK32
+    for _ in range(10):
+        p0 = np.uint64(_PHILOX_M0) * c[0]
+        p1 = np.uint64(_PHILOX_M1) * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(_MASK32)
+        hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(_MASK32)
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+        k0 = (k0 + np.uint64(_PHILOX_W0)) & np.uint64(_MASK32)
+        k1 = (k1 + np.uint64(_PHILOX_W1)) & np.uint64(_MASK32)
+    return np.stack(c, axis=-1).astype(np.uint32)
+
+
+def dropout_threshold(p_drop: float) -> int:
+    """Keep threshold t on a random byte: keep iff byte < t, with
+    t = round(256 (1 - p_drop)) clamped to [1, 256]; the kept weights are
+    scaled by 256 / t, so the expected output is the undropped one."""
+    return int(min(256, max(1, round(256.0 * (1.0 - p_drop)))))
+
+
+def dropout_keep(bh: int, nq: int, nk: int, p_drop: float, seed: int, offset: int):
+    """Keep mask [nq, nk] of one (batch, head) index bh.  Element (i, j) takes
+    byte j % 4 (bits 8 (j % 4) .. 8 (j % 4) + 7) of output word i % 4 of
+    Philox4x32-10 with counter (j // 4, i // 4, bh, offset) and key
+    (seed mod 2^32, seed div 2^32): one call covers a 4 x 4 patch."""
+    qi, kj = np.meshgrid(np.arange(nq), np.arange(nk), indexing="ij")
+    ctr = np.stack([kj // 4, qi // 4, np.full_like(qi, bh), np.full_like(qi, offset)], axis=-1)
+    key = np.array([seed & _MASK32, (seed >> 32) & _MASK32], dtype=np.uint64)
+    words = philox4x32_10(ctr.astype(np.uint64), key)
+    w = np.take_along_axis(words, (qi % 4)[..., None], axis=-1)[..., 0].astype(np.uint64)
+    byte = (w >> (8 * (kj % 4)).astype(np.uint64)) & np.uint64(0xFF)
+    return byte < np.uint64(dropout_threshold(p_drop))
+
+
+def attention_forward_dropout(q, k, v, causal: bool, scale: float, keep, p_drop: float):
+    """O and lse of one head with dropout applied to P (sj-techlog page,
+    backward section; FlashAttention's dropout on the softmax output):
+    O = (P o Z) V * 256 / t with Z the keep mask and t the keep threshold;
+    lse is that of the undropped softmax."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nq, nk = len(q), len(k)
+    vis = np.ones((nq, nk), bool)
+    if causal:
+        vis = np.arange(nk)[None, :] <= np.arange(nq)[:, None]
+    s = np.where(vis, scale * (q @ k.T), -np.inf)
+    m = s.max(axis=1)
+    e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    z = e.sum(axis=1)
+    p = e / z[:, None]
+    w = 256.0 / dropout_threshold(p_drop)
+    return (p * np.asarray(keep)) @ v * w, m + np.log(z)
+
+
+def attention_backward_dropout(q, k, v, dO, causal: bool, scale: float, keep, p_drop: float):
+    """(dQ, dK, dV) of attention_forward_dropout: with P~ = P o Z * w
+    (w = 256 / t), dV = P~^T dO, dP = Z o (dO V^T) * w, D_i = sum_j P_ij dP_ij
+    (= rowsum(dO o O)), dS = P o (dP - D), dQ = tau dS K, dK = tau dS^T Q."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    nq, nk = len(q), len(k)
+    vis = np.ones((nq, nk), bool)
+    if causal:
+        vis = np.arange(nk)[None, :] <= np.arange(nq)[:, None]
+    s = np.where(vis, scale * (q @ k.T), -np.inf)
+    m = s.max(axis=1)
+    e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    p = e / e.sum(axis=1)[:, None]
+    zw = np.asarray(keep) * (256.0 / dropout_threshold(p_drop))
+    dv = (p * zw).T @ dO
+    dp = (dO @ v.T) * zw
+    D = (p * dp).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), dv

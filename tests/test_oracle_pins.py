@@ -573,3 +573,84 @@ def test_backward_given_stats_sums_to_full_backward(causal):
     own = oracle.attention_backward_given_stats(q, k, v, dO, lse, D, causal, tau)
     for a, b in zip(own, (dq, dk, dv)):
         assert np.max(np.abs(a - b)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Dropout: the generator, the mask layout and dropout attention
+# --------------------------------------------------------------------------
+
+def test_philox_known_answers():
+    g = _golden("philox4x32_10_kat.json")
+    for vec in g["vectors"]:
+        ctr = np.array([int(x, 16) for x in vec["counter"]], dtype=np.uint64)
+        key = np.array([int(x, 16) for x in vec["key"]], dtype=np.uint64)
+        out = oracle.philox4x32_10(ctr, key)
+        assert [int(x) for x in out] == [int(x, 16) for x in vec["output"]]
+
+
+def test_dropout_mask_layout_and_rate():
+    """Element (i, j) is byte j % 4 of word i % 4 of the call with counter
+    (j // 4, i // 4, bh, offset); the keep rate matches t / 256; other
+    offsets, heads and seeds give other masks."""
+    p, seed, off = 0.3, 0x1234_5678_9ABC, 7
+    keep = oracle.dropout_keep(5, 64, 96, p, seed, off)
+    t = oracle.dropout_threshold(p)
+    assert t == 179
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint64)
+    # element by element, one generator call each, over a 16 x 12 corner
+    # and the far corner (a swapped word / byte index fails both)
+    for (i0, j0) in ((0, 0), (48, 84)):
+        for i in range(i0, i0 + 16):
+            for j in range(j0, j0 + 12):
+                w = oracle.philox4x32_10(np.array([j // 4, i // 4, 5, off], dtype=np.uint64), key)
+                byte = (int(w[i % 4]) >> (8 * (j % 4))) & 0xFF
+                assert keep[i, j] == (byte < t), (i, j)
+    big = oracle.dropout_keep(1, 512, 512, p, seed, off)
+    n = big.size
+    rate = big.mean()
+    assert abs(rate - t / 256) < 5 * np.sqrt(t / 256 * (1 - t / 256) / n)
+    for other in (oracle.dropout_keep(2, 512, 512, p, seed, off),
+                  oracle.dropout_keep(1, 512, 512, p, seed, off + 1),
+                  oracle.dropout_keep(1, 512, 512, p, seed + 1, off)):
+        agree = (other == big).mean()
+        expect = rate * rate + (1 - rate) * (1 - rate)
+        assert abs(agree - expect) < 0.01
+    assert oracle.dropout_threshold(0.0) == 256 and oracle.dropout_keep(0, 9, 9, 0.0, 1, 2).all()
+    assert oracle.dropout_threshold(0.999) == 1
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_zero_is_plain_attention(causal):
+    r = _rng(100 + int(causal))
+    q, k, v, dO = (r.normal(size=(9, 3)) for _ in range(4))
+    keep = np.ones((9, 9), bool)
+    o, lse = oracle.attention_forward_dropout(q, k, v, causal, 0.7, keep, 0.0)
+    o2, lse2 = oracle.attention_forward(q, k, v, causal, 0.7)
+    assert np.max(np.abs(o - o2)) < 1e-13 and np.max(np.abs(lse - lse2)) < 1e-13
+    got = oracle.attention_backward_dropout(q, k, v, dO, causal, 0.7, keep, 0.0)
+    want = oracle.attention_backward(q, k, v, dO, causal, 0.7)[:3]
+    for a, b in zip(got, want):
+        assert np.max(np.abs(a - b)) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_backward_matches_finite_differences(causal):
+    """With the keep mask held fixed, central differences of L = sum(dO * O);
+    p = 0.3 (scale 256 / 179), d != dv, and the kept set is a real mask."""
+    r = _rng(110 + int(causal))
+    n, tau, p = 7, 0.7, 0.3
+    q, k = r.normal(size=(n, 3)), r.normal(size=(n, 3))
+    v, dO = r.normal(size=(n, 2)), r.normal(size=(n, 2))
+    keep = oracle.dropout_keep(3, n, n, p, 99, 1)
+    assert 0 < keep.sum() < keep.size
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward_dropout(qq, kk, vv, causal, tau, keep, p)
+        return float(np.sum(o * dO))
+
+    dq, dk, dv = oracle.attention_backward_dropout(q, k, v, dO, causal, tau, keep, p)
+    for got, want in ((dq, _fd_grad(q, lambda x: loss(x, k, v))),
+                      (dk, _fd_grad(k, lambda x: loss(q, x, v))),
+                      (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
