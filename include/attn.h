@@ -364,6 +364,46 @@ int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO
                      float* dv32, int accumulate, int B, int H, int Hkv, int N, int d,
                      int causal, float scale, void* stream);
 
+/*
+ * Dropout on the attention probabilities, training path (sj-techlog page,
+ * backward section: the forward keeps the pseudo-random generator's state,
+ * and the backward regenerates the same dropout mask from it instead of
+ * storing an N x N mask).  The generator is Philox4x32-10 (Salmon, Moraes,
+ * Dror, Shaw, SC'11), written from its definition.
+ *  - Mask: element (query i, key j) of (batch, head) index bh = b * H + h is
+ *    kept iff byte j % 4 (bits 8 (j % 4) .. + 7) of output word i % 4 of
+ *    Philox4x32-10 with counter (j / 4, i / 4, bh, offset) and key
+ *    (seed mod 2^32, seed / 2^32) is below t = 256 (1 - p_drop) rounded half
+ *    to even and clamped to [1, 256].  One generator call covers a 4 x 4
+ *    patch.  t = 256 keeps everything (then identical to the plain entry
+ *    points).  p_drop must be in [0, 1), else ATTN_ERR_INVALID_ARG.
+ *  - Forward: O = (P o Z) V * 256 / t, with P the undropped softmax; lse is
+ *    that of the undropped softmax; o32 as for attn_fwd_train (normalised by
+ *    the sum of the rounded, undropped probabilities, then scaled).
+ *  - Backward: D from attn_bwd_preprocess_o32 of that o32 (rowsum(dO o O));
+ *    then with the same p_drop, seed and offset, dV = (P o Z)^T dO * 256 / t,
+ *    dP = Z o (dO V^T) * 256 / t, dS = P o (dP - D), dQ = tau dS K,
+ *    dK = tau dS^T Q.
+ *  - Dense layout, one K / V head per query head.  Other conventions as for
+ *    attn_fwd_train and attn_bwd.  Calls with another offset (or seed) draw
+ *    an independent mask.
+ */
+int attn_fwd_train_dropout(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, float p_drop, unsigned long long seed, unsigned int offset,
+                           int B, int H, int N, int d, int causal, float scale, void* stream);
+int attn_fwd_train_dropout_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                               float* lse, float p_drop, unsigned long long seed,
+                               unsigned int offset, int B, int H, int N, int d, int causal,
+                               float scale, void* stream);
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                     void* dv, float p_drop, unsigned long long seed, unsigned int offset, int B,
+                     int H, int N, int d, int causal, float scale, void* stream);
+int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                         void* dv, float p_drop, unsigned long long seed, unsigned int offset,
+                         int B, int H, int N, int d, int causal, float scale, void* stream);
+
 /* Static English description of a status code. */
 const char* attn_status_string(int status);
 

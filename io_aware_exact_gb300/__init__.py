@@ -112,6 +112,16 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = [P, P, LL, F, P]
                 fn.restype = I
+            # dropout: (p_drop, seed, offset) before B
+            U64, U32 = ctypes.c_ulonglong, ctypes.c_uint
+            for name in ("attn_fwd_train_dropout", "attn_fwd_train_dropout_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, P, P, P, F, U64, U32, I, I, I, I, I, F, P]
+                fn.restype = I
+            for name in ("attn_bwd_dropout", "attn_bwd_dropout_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, P, P, P, P, P, P, P, F, U64, U32, I, I, I, I, I, F, P]
+                fn.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -403,6 +413,47 @@ def convert(x, dtype, scale: float = 1.0, out=None, stream=None):
     _check(fn(x.data_ptr(), out.data_ptr(), x.numel(), float(scale), _stream_handle(stream)),
            "attn_convert")
     return out
+
+
+def forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0, causal: bool = False,
+                    scale=None, o=None, lse=None, o32=None, stream=None):
+    """Training forward with dropout on P (mask regenerated from seed, offset):
+    returns (o, lse, o32) for [B,H,N,d] tensors."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device) if o32 is None else o32
+    fn = lib().attn_fwd_train_dropout_f16 if f16 else lib().attn_fwd_train_dropout
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o32.data_ptr(),
+              lse.data_ptr(), float(p_drop), int(seed), int(offset), B, H, N, d,
+              int(bool(causal)), scale, _stream_handle(stream)), "attn_fwd_train_dropout")
+    return o, lse, o32
+
+
+def backward_dropout(q, k, v, o32, lse, dO, p_drop: float, seed: int, offset: int = 0,
+                     causal: bool = False, scale=None, dq=None, dk=None, dv=None, D=None,
+                     dq_accum=None, stream=None):
+    """dQ, dK, dV of forward_dropout with the same p_drop, seed and offset."""
+    torch = _torch()
+    (B, H, N, d), f16 = _check_qkv(q, k, v, dO)
+    scale = d ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    D = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if D is None else D
+    if dq_accum is None:
+        dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    s = _stream_handle(stream)
+    attn_bwd_preprocess_o32(o32.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(),
+                            B, H, N, d, s, f16)
+    fn = lib().attn_bwd_dropout_f16 if f16 else lib().attn_bwd_dropout
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+              float(p_drop), int(seed), int(offset), B, H, N, d, int(bool(causal)), scale, s),
+           "attn_bwd_dropout")
+    return dq, dk, dv
 
 
 def _autograd_function():

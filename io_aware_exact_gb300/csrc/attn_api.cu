@@ -160,9 +160,24 @@ int check_sparse(const void* block_mask, long long mask_stride, int H, int Hkv, 
     return ATTN_OK;
 }
 
+// Dropout settings from the drop probability: keep iff a random byte is below
+// t = 256 (1 - p) rounded half to even, clamped to [1, 256]; t = 256 keeps all.
+int make_dropout(float p_drop, unsigned long long seed, unsigned int offset, DropoutArgs* out) {
+    if (!std::isfinite(p_drop) || p_drop < 0.f || p_drop >= 1.f) return ATTN_ERR_INVALID_ARG;
+    double t = std::nearbyint(256.0 * (1.0 - static_cast<double>(p_drop)));
+    t = t < 1.0 ? 1.0 : (t > 256.0 ? 256.0 : t);
+    out->seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
+    out->seed_hi = static_cast<uint32_t>(seed >> 32);
+    out->offset = offset;
+    out->drop_t = static_cast<uint32_t>(t);
+    out->drop_scale = static_cast<float>(256.0 / t);
+    return ATTN_OK;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse, int B,
              int H, int Hkv, int N, int d, int causal, float scale, void* stream, bool bf16,
-             const void* block_mask = nullptr, long long mask_stride = 0) {
+             const void* block_mask = nullptr, long long mask_stride = 0,
+             const DropoutArgs* drop = nullptr) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (o32 != nullptr && !aligned16(o32)) return ATTN_ERR_MISALIGNED;
     int rc = check_shape(B, H, N, d);
@@ -200,6 +215,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, f
     a.block_mask = static_cast<const uint8_t*>(block_mask);
     a.mask_head_stride = mask_stride;
     a.mask_cols = (N + kTile - 1) / kTile;
+    if (drop != nullptr) a.drop = *drop;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_fwd(tq, tk, tv, to, to32, a, BH, d, causal != 0, bf16,
@@ -262,7 +278,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
              const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int Hkv,
              int N, int d, int causal, float scale, void* stream, bool bf16,
              const void* block_mask = nullptr, long long mask_stride = 0,
-             float* dk32 = nullptr, float* dv32 = nullptr, int acc32 = 0) {
+             float* dk32 = nullptr, float* dv32 = nullptr, int acc32 = 0,
+             const DropoutArgs* drop = nullptr) {
     // with fp32 gradient outputs (dk32, dv32) the 16-bit dk, dv are not used
     const bool f32 = dk32 != nullptr || dv32 != nullptr;
     if (f32 && (!dk32 || !dv32)) return ATTN_ERR_INVALID_ARG;
@@ -315,6 +332,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.dk32 = dk32;
     a.dv32 = dv32;
     a.acc32 = acc32;
+    if (drop != nullptr) a.drop = *drop;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -827,6 +845,51 @@ int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO
     if (!dk32 || !dv32) return ATTN_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, nullptr, nullptr, B, H, Hkv, N, d, causal,
                     scale, stream, false, nullptr, 0, dk32, dv32, accumulate != 0);
+}
+
+int attn_fwd_train_dropout(const void* q, const void* k, const void* v, void* o, float* o32,
+                           float* lse, float p_drop, unsigned long long seed, unsigned int offset,
+                           int B, int H, int N, int d, int causal, float scale, void* stream) {
+    DropoutArgs dr{};
+    int rc = make_dropout(p_drop, seed, offset, &dr);
+    if (rc) return rc;
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true, nullptr, 0,
+                    &dr);
+}
+
+int attn_fwd_train_dropout_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                               float* lse, float p_drop, unsigned long long seed,
+                               unsigned int offset, int B, int H, int N, int d, int causal,
+                               float scale, void* stream) {
+    DropoutArgs dr{};
+    int rc = make_dropout(p_drop, seed, offset, &dr);
+    if (rc) return rc;
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false, nullptr, 0,
+                    &dr);
+}
+
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                     void* dv, float p_drop, unsigned long long seed, unsigned int offset, int B,
+                     int H, int N, int d, int causal, float scale, void* stream) {
+    DropoutArgs dr{};
+    int rc = make_dropout(p_drop, seed, offset, &dr);
+    if (rc) return rc;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
+                    stream, true, nullptr, 0, nullptr, nullptr, 0, &dr);
+}
+
+int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                         void* dv, float p_drop, unsigned long long seed, unsigned int offset,
+                         int B, int H, int N, int d, int causal, float scale, void* stream) {
+    DropoutArgs dr{};
+    int rc = make_dropout(p_drop, seed, offset, &dr);
+    if (rc) return rc;
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
+                    stream, false, nullptr, 0, nullptr, nullptr, 0, &dr);
 }
 
 int attn_convert(const float* x, void* y, long long elems, float scale, void* stream) {

@@ -432,7 +432,7 @@ __device__ __forceinline__ uint32_t dq_box_addr(uint32_t sbase, int s, int b) {
            (b % per_tile) * C::DQ_BOX_BYTES;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -791,6 +791,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const bool key_ok = key < N;
                 uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
                 float pv[64];        // P^T of this key row, query columns [64c, 64c + 64), fp32
+                // dropout: keep bits of this key row for query columns [64c + 32 ch, +32)
+                uint32_t kbits[2] = {0u, 0u};
                 // P^T_i: wait for S^T_i and block i's statistics, write packed P^T to TMEM
                 auto compute_p = [&](int it) -> bool {
                     const int s = it % C::STAGES;
@@ -811,6 +813,30 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // masked columns of this chunk are those below lim (the query
                         // precedes the key; all of them past the key tail)
                         const int lim = key_ok ? key - (qbase + 32 * ch) : 32;
+                        if constexpr (DROPOUT) {
+                            // one generator call per lane and 16 query columns: patch
+                            // (key patch of the lane's group, query patch), transposed so
+                            // that word b holds key column b, then exchanged so that each
+                            // lane holds its key's bytes; bit q of kbits = query column q
+                            const uint32_t kp = static_cast<uint32_t>((j * kTile + wq * 32) >> 2) + (lane >> 2);
+                            const uint32_t t4 = args.drop.drop_t * 0x01010101u;
+                            uint32_t bits = 0u;
+        #pragma unroll
+                            for (int g = 0; g < 2; ++g) {
+                                const uint4 w = philox4x32_10(
+                                    make_uint4(kp, static_cast<uint32_t>((qbase + 32 * ch) >> 2) + (lane & 3) + 4 * g,
+                                               static_cast<uint32_t>(bkv), args.drop.offset),
+                                    args.drop.seed_lo, args.drop.seed_hi);
+                                uint32_t rv[4];
+                                exchange_patch_words(transpose_bytes(w), lane, rv);
+        #pragma unroll
+                                for (int cpp = 0; cpp < 4; ++cpp) {
+                                    const uint32_t m4 = __vcmpltu4(rv[cpp], t4) & 0x08040201u;
+                                    bits |= ((m4 * 0x01010101u) >> 24) << (16 * g + 4 * cpp);
+                                }
+                            }
+                            kbits[ch] = bits;
+                        }
                         uint32_t sr[32];
                         tmem_ld_sync(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
         #pragma unroll
@@ -833,6 +859,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                 pv[32 * ch + q] = p0;
                                 pv[32 * ch + q + 1] = p1;
                                 pp[16 * ch + 2 * e4 + u] = pack2<BF16>(p0, p1);
+                                if constexpr (DROPOUT) {   // dV takes the kept P only
+                                    const uint32_t b2 = (kbits[ch] >> q) & 3u;
+                                    pp[16 * ch + 2 * e4 + u] &= ((b2 & 1u) * 0xFFFFu) | ((b2 >> 1) * 0xFFFF0000u);
+                                }
                             }
                         }
                     }
@@ -861,9 +891,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int q = 4 * e4 + 2 * u;
+                                uint64_t dp2 = f2_pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1]));
+                                if constexpr (DROPOUT) {   // dP = Z o (dO V^T) * 256 / t
+                                    const uint32_t b2 = (kbits[ch] >> q) & 3u;
+                                    const float w = args.drop.drop_scale;
+                                    dp2 = f2_mul(dp2, f2_pack((b2 & 1u) ? w : 0.f, (b2 & 2u) ? w : 0.f));
+                                }
                                 const uint64_t dsv = f2_mul(f2_pack(pv[32 * ch + q], pv[32 * ch + q + 1]),
-                                                            f2_add(f2_pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1])),
-                                                                   nd2[u]));
+                                                            f2_add(dp2, nd2[u]));
                                 float d0, d1;
                                 f2_unpack(dsv, d0, d1);
                                 pd[16 * ch + 2 * e4 + u] = pack2<BF16>(d0, d1);
@@ -921,7 +956,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
                 if (ok) {
                     tc_fence_after();
-                    const float mul = (c == 0) ? 1.0f : args.scale;
+                    // dV summed the kept P unscaled: apply 256 / t here under dropout
+                    const float mul = (c == 0) ? (DROPOUT ? args.drop.drop_scale : 1.0f) : args.scale;
                     const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
                     const int region = (c == 0) ? C::V_OFF : C::K_OFF;
                     uint8_t* stage_row = smem + region + r * 128;
@@ -1033,12 +1069,12 @@ cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t st
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE = false>
+template <int D, bool CAUSAL, bool BF16, bool GENERAL, bool SPARSE = false, bool DROPOUT = false>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                                 const CUtensorMap& tdv, const BwdArgs& a, int BH, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GENERAL, SPARSE>;
+    auto kern = attn_bwd_kernel<D, CAUSAL, BF16, GENERAL, SPARSE, DROPOUT>;
     constexpr int smem = SPARSE ? C::SMEM_SPARSE : C::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1089,10 +1125,13 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr || a.num_kvblocks > kMaxGridY ||
                          a.dk32 != nullptr;
     const bool sparse = a.block_mask != nullptr;   // dense layout, Hkv = H only
-    if (sparse && general) return cudaErrorInvalidValue;
+    const bool dropout = a.drop.drop_t > 0 && a.drop.drop_t < 256;   // dense layout, Hkv = H only
+    if ((sparse || dropout) && general) return cudaErrorInvalidValue;
+    if (sparse && dropout) return cudaErrorInvalidValue;
 #define ATTN_BWD_CASE(D_, C_, B_)                                                              \
     if (d == D_ && causal == C_ && bf16 == B_)                                                 \
-        return sparse ? launch_bwd_t<D_, C_, B_, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+        return dropout ? launch_bwd_t<D_, C_, B_, false, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
+             : sparse ? launch_bwd_t<D_, C_, B_, false, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
              : general ? launch_bwd_t<D_, C_, B_, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream) \
                        : launch_bwd_t<D_, C_, B_, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, BH, stream);
     ATTN_BWD_CASE(64, false, true)

@@ -23,6 +23,17 @@ constexpr int kBoxBytes = kTile * kBoxCols * 2;  // 16 KB
 // most this many (N <= 384 * 128 = 49,152); list entries are 16-bit.
 constexpr int kMaxSparseBlocks = 384;
 
+// Dropout (training forward and backward): the keep mask is regenerated
+// from (seed, offset) in both passes, never stored.  Element (i, j) of head
+// bh keeps iff byte j % 4 of word i % 4 of Philox4x32-10 with counter
+// (j / 4, i / 4, bh, offset) and key (seed_lo, seed_hi) is below drop_t; kept
+// weights are scaled by drop_scale = 256 / drop_t.
+struct DropoutArgs {
+    uint32_t seed_lo, seed_hi, offset;
+    uint32_t drop_t;       // 1..255 (256, no dropout, uses the kernels without it)
+    float drop_scale;      // 256 / drop_t
+};
+
 struct FwdArgs {
     void* o;               // [B*H, N, d] 16-bit, written
     float* o32;            // [B*H, N, d] fp32 copy of O for the backward, or nullptr
@@ -46,6 +57,7 @@ struct FwdArgs {
     const uint8_t* block_mask;
     long long mask_head_stride;
     int mask_cols;
+    DropoutArgs drop;      // used by the dropout instantiations only
     float scale_log2;      // softmax scale * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
 };
@@ -78,6 +90,7 @@ struct BwdArgs {
     float* dk32;
     float* dv32;
     int acc32;
+    DropoutArgs drop;      // used by the dropout instantiations only
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
     unsigned int wait_polls;   // try_wait polls before a wait gives up (about 2 us each)
@@ -191,6 +204,53 @@ inline int device_sm_count() {
 // K / V head of (batch, query head) bh when groups of H / Hkv query heads share one
 __device__ __forceinline__ int kv_head(int bh, int H, int Hkv) {
     return (bh / H) * Hkv + (bh % H) / (H / Hkv);
+}
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC'11): each round maps (c0, c1, c2, c3) with
+// key (k0, k1) to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+// lo(M0 c0)), and the key is bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint32_t sel4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int i) {
+    return i == 0 ? a : i == 1 ? b : i == 2 ? c : d;
+}
+
+// Keep masks of one 4 x 4 patch exchanged inside a group of four lanes.
+// Lane L of the group computes the patch at position (L & 3) + 4m of a row of
+// patches (four words w, word a = patch row a, byte b = patch column b), and
+// needs word `want` of every patch of that row: in round rr it receives, from
+// lane (L & 3) + rr of its group, the word of patch ((L & 3) + rr) & 3 + 4m
+// (the source sends its word (its lane - rr) & 3).  Returned in rv[cpp] for
+// patch cpp + 4m, cpp = 0..3.
+__device__ __forceinline__ void exchange_patch_words(uint4 w, int lane, uint32_t (&rv)[4]) {
+    const int l = lane & 3;
+    uint32_t got[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const uint32_t send = sel4(w.x, w.y, w.z, w.w, (l - rr) & 3);
+        got[rr] = __shfl_sync(0xffffffffu, send, (lane & ~3) | ((l + rr) & 3));
+    }
+#pragma unroll
+    for (int cpp = 0; cpp < 4; ++cpp) rv[cpp] = sel4(got[0], got[1], got[2], got[3], (cpp - l) & 3);
+}
+
+// 4 x 4 byte transpose: result word b holds byte b of w.x, w.y, w.z, w.w.
+__device__ __forceinline__ uint4 transpose_bytes(uint4 w) {
+    const uint32_t t0 = __byte_perm(w.x, w.y, 0x5140), t1 = __byte_perm(w.x, w.y, 0x7362);
+    const uint32_t t2 = __byte_perm(w.z, w.w, 0x5140), t3 = __byte_perm(w.z, w.w, 0x7362);
+    return make_uint4(__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                      __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632));
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -68,7 +68,7 @@ struct FwdCfg {
     static_assert(SMEM_SPARSE <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -381,6 +381,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     #pragma unroll
                 for (int h = 0; h < 128 / PW; ++h) {
                     uint32_t pk[PW / 2];
+                    // dropout keep bytes of these columns: one generator call per lane
+                    // and 16-column group, exchanged so that each lane holds its row's
+                    // bytes (patch row = its row % 4); then 0xFF per kept byte
+                    uint32_t keep4[PW / 16][4];
+                    if constexpr (DROPOUT) {
+                        const uint32_t rp = static_cast<uint32_t>((q0 + kTile * t + 32 * wq) >> 2) + (lane >> 2);
+                        const uint32_t t4 = args.drop.drop_t * 0x01010101u;
+    #pragma unroll
+                        for (int g = 0; g < PW / 16; ++g) {
+                            const int m = (PW / 16) * h + g;
+                            const uint4 w = philox4x32_10(
+                                make_uint4(static_cast<uint32_t>(j * 32 + (lane & 3) + 4 * m), rp,
+                                           static_cast<uint32_t>(bh), args.drop.offset),
+                                args.drop.seed_lo, args.drop.seed_hi);
+                            exchange_patch_words(w, lane, keep4[g]);
+    #pragma unroll
+                            for (int cpp = 0; cpp < 4; ++cpp) keep4[g][cpp] = __vcmpltu4(keep4[g][cpp], t4);
+                        }
+                    }
     #pragma unroll
                     for (int e = 0; e < PW / 2; ++e) {
                         const uint64_t arg = f2_fma(f2_pack(sv[PW * h + 2 * e], sv[PW * h + 2 * e + 1]), cs2, nm2);
@@ -391,6 +410,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         sum2 = f2_add(sum2, f2_pack(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
                         if constexpr (TRAIN) add_halves<BF16>(sumb0, sumb1, pk[e]);
+                        if constexpr (DROPOUT)   // zero the dropped halves; lb keeps them
+                            pk[e] &= __byte_perm(keep4[e / 8][(e % 8) / 2], 0u, (e & 1) ? 0x3322 : 0x1100);
                     }
                     if constexpr (TRAIN)
                         tmem_st16(s_addr + PW / 2 * h, pk);
@@ -435,7 +456,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float den = TRAIN ? lb : l;
                 // (block-sparse: a row whose kept tiles were all above the
                 // diagonal has an empty softmax, O = 0)
-                const float inv_l = (SPARSE && !(den > 0.f)) ? 0.f : 1.0f / den;
+                // (dropout: the kept weights are scaled by 256 / t)
+                const float inv_l = (SPARSE && !(den > 0.f)) ? 0.f
+                                    : (DROPOUT ? args.drop.drop_scale : 1.0f) / den;
                 const bool issuer = (warp & 3) == 0 && lane == 0;
                 const uint32_t stage = sbase + C::Q_OFF + t * C::TILE_BYTES;
                 uint8_t* stage_row = smem + C::Q_OFF + t * C::TILE_BYTES + r * 128;
@@ -547,13 +570,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE = false>
+template <int D, bool CAUSAL, bool BF16, bool TRAIN, bool VARLEN, bool SPARSE = false,
+          bool DROPOUT = false>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to,
                                 const CUtensorMap& to32, const FwdArgs& a, int BH,
                                 cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN, VARLEN, SPARSE>;
+    auto kern = attn_fwd_kernel<D, CAUSAL, BF16, TRAIN, VARLEN, SPARSE, DROPOUT>;
     constexpr int smem = SPARSE ? C::SMEM_SPARSE : C::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -568,8 +592,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        int d, bool causal, bool bf16, cudaStream_t stream) {
     const bool varlen = a.cu_seqlens != nullptr;
     const bool sparse = a.block_mask != nullptr;
+    const bool dropout = a.drop.drop_t > 0 && a.drop.drop_t < 256;   // training path, dense only
+    if (dropout && (varlen || sparse || a.o32 == nullptr)) return cudaErrorInvalidValue;
 #define ATTN_FWD_CASE(D_, C_, B_)                                                                   \
     if (d == D_ && causal == C_ && bf16 == B_) {                                                    \
+        if (dropout)                                                                                \
+            return launch_fwd_t<D_, C_, B_, true, false, false, true>(tq, tk, tv, to, to32, a, BH, stream); \
         if (sparse)                                                                                 \
             return a.o32 != nullptr ? launch_fwd_t<D_, C_, B_, true, false, true>(tq, tk, tv, to, to32, a, BH, stream) \
                                     : launch_fwd_t<D_, C_, B_, false, false, true>(tq, tk, tv, to, to32, a, BH, stream); \

@@ -237,3 +237,21 @@ def test_combine_entry_points_argument_errors(L):
     assert L.attn_convert(A, A, 12, 1.0, None) == 1       # not a multiple of 8
     assert L.attn_convert(A, A, 64, float("nan"), None) == 1
     assert L.attn_convert_f16(A, None, 64, 1.0, None) == 1
+
+
+def test_dropout_argument_errors(L):
+    def fwd(p=0.1, o32=A, **kw):
+        return L.attn_fwd_train_dropout(A, A, A, A, o32, A, p, 123, 4, 1, 2, kw.get("N", 256),
+                                        kw.get("d", 64), 1, 0.125, None)
+
+    def bwd(p=0.1, dk=A):
+        return L.attn_bwd_dropout(A, A, A, A, A, A, A, A, dk, A, p, 123, 4, 1, 2, 256, 64, 1,
+                                  0.125, None)
+
+    assert fwd() in (0, 4) and fwd(p=0.0) in (0, 4) and bwd() in (0, 4)
+    for bad in (1.0, 1.5, -0.1, float("nan"), float("inf")):
+        assert fwd(p=bad) == 1 and bwd(p=bad) == 1
+    assert fwd(o32=None) == 1
+    assert fwd(d=96) == 2
+    assert bwd(dk=None) == 1
+    assert bwd(dk=A + 2) == 3
