@@ -663,6 +663,80 @@ def run_ring(args):
     }))
 
 
+def run_dropout(args):
+    """The causal B=2 H=16 N=8192 d=128 training step (Q and K x3) with
+    dropout p = --dropout on the attention probabilities: the mask is
+    regenerated in the forward and the backward from (seed, offset), a new
+    offset every step.  FLOPs as for the dense causal step; the step without
+    dropout on the same inputs is timed beside it."""
+    import torch
+    import io_aware_exact_gb300 as attn
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[HEADLINE]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    x = {n: t.to(dev) for n, t in make_inputs(B, H, N, d, seed=w.seed, qk_mult=w.qk_mult).items()}
+    q, k, v, dO = x["q"], x["k"], x["v"], x["dO"]
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    seed = 0x5EED
+
+    def drop_step(i, mid):
+        attn.forward_dropout(q, k, v, args.dropout, seed, i, True, scale, o=o, lse=lse, o32=o32,
+                             stream=stream)
+        mid.record(stream)
+        attn.backward_dropout(q, k, v, o32, lse, dO, args.dropout, seed, i, True, scale, dq=dq,
+                              dk=dk, dv=dv, D=D, dq_accum=acc, stream=stream)
+
+    def plain_step(i, mid):
+        attn.forward(q, k, v, True, scale, o=o, lse=lse, o32=o32, stream=stream)
+        mid.record(stream)
+        attn.backward(q, k, v, None, lse, dO, True, scale, dq=dq, dk=dk, dv=dv, D=D,
+                      dq_accum=acc, stream=stream, o32=o32)
+
+    def timed(step):
+        for i in range(args.warmup):
+            step(i, torch.cuda.Event())
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step(args.warmup + i, evs[i][2])
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        if attn.attn_get_device_status() != 0:
+            raise RuntimeError("device status set during the dropout steps")
+        return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                statistics.mean(e[0].elapsed_time(e[2]) for e in evs))
+
+    with ClockSampler(0) as clk:
+        ms, ms_fwd = timed(drop_step)
+        ms_plain, ms_plain_fwd = timed(plain_step)
+    flops = 10.0 * B * H * N * N * d / 2
+    peak = _peaks().get("bf16_tflops_sustained")
+    value = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "attention TFLOPS fwd+bwd with dropout on P",
+        "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), Q and K x3)",
+        "config": {"workload": "dropout_causal_b2_h16_n8192_d128", "p_drop": args.dropout,
+                   "l2": "L2 flushed (512 MB write) between steps"},
+        "frac_of_peak": round(value / peak, 4) if peak else None,
+        "fwd_train_ms": round(ms_fwd, 4), "bwd_ms": round(ms - ms_fwd, 4),
+        "no_dropout_step_ms": round(ms_plain, 4), "no_dropout_fwd_train_ms": round(ms_plain_fwd, 4),
+        "clocks": clk.summary(),
+    }))
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, timed on the host cores.
 
@@ -730,6 +804,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--varlen", action="store_true",
                     help="time the step on a packed variable-length batch instead")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="time the step with dropout of this probability on P instead")
     ap.add_argument("--ring", type=int, default=0,
                     help="time the step as ring attention over this many chunks, emulated "
                          "on one GPU, instead")
@@ -745,6 +821,8 @@ def main():
         run_bsparse(args)
     elif args.ring > 0:
         run_ring(args)
+    elif args.dropout > 0:
+        run_dropout(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
