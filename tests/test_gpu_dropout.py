@@ -48,7 +48,6 @@ def test_dropout_matches_oracle(B, H, N, d, causal, p, dtype):
     x = make_inputs(B, H, N, d, seed=800 + N + d, dtype=dtype)
     offset = 17
     out = _run(x, p, SEED, offset, causal, scale)
-    H_all = B * H
     for b in range(B):
         for h in range(H):
             bh = b * H + h
@@ -61,7 +60,6 @@ def test_dropout_matches_oracle(B, H, N, d, causal, p, dtype):
             for n, ref in (("o", o_ref), ("o32", o_ref), ("dq", dq_ref), ("dk", dk_ref),
                            ("dv", dv_ref)):
                 check_tensor(n, _f64(out[n][b, h]), ref)
-    assert H_all == B * H
 
 
 def test_dropout_zero_is_the_plain_training_path():
