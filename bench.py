@@ -162,6 +162,10 @@ def run_ours(args):
     s = int(stream.cuda_stream)
     scale = w.scale
     P = lambda t: t.data_ptr()
+    # grouped heads: the group split over CTAs as the library suggests
+    splits = int(attn.lib().attn_gqa_split_hint(B, H, Hkv, N, int(causal))) if Hkv != H else 1
+    part = (torch.empty((2, splits, B, Hkv, N, d), dtype=torch.float32, device=dev)
+            if splits > 1 else None)
 
     def step(ev=None):
         if ev:
@@ -173,8 +177,13 @@ def run_ours(args):
         attn.attn_bwd_preprocess_o32(P(o32), P(dO), P(D), P(acc), B, H, N, d, s)
         if ev:
             ev[2].record(stream)
-        attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
-                      B, H, N, d, causal, scale, s, Hkv=Hkv)
+        if splits > 1:
+            attn._check(attn.lib().attn_bwd_gqa_split(
+                P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv), P(part), splits,
+                B, H, Hkv, N, d, int(causal), scale, s), "attn_bwd_gqa_split")
+        else:
+            attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
+                          B, H, N, d, causal, scale, s, Hkv=Hkv)
         if ev:
             ev[3].record(stream)
 
@@ -333,7 +342,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), Q and K x3, bf16)",
-        "config": {"workload": workload, "B": B, "H": H, "kv_heads": Hkv, "N": N, "d": d,
+        "config": {"workload": workload, "B": B, "H": H, "kv_heads": Hkv, "gqa_splits": splits,
+                   "N": N, "d": d,
                    "causal": causal,
                    "global_batch": B * world, "seq_len": N,
                    "parallelism": "replicas" if world > 1 else "single",

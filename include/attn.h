@@ -210,6 +210,31 @@ int attn_bwd_gqa_f16(const void* q, const void* k, const void* v, const void* dO
                      int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * Grouped heads with the group split over CTAs.  attn_bwd_gqa runs one CTA
+ * per (batch, K / V head, key block) that loops over all query heads of the
+ * group, so with few K / V heads a few CTAs carry most of the work.  This
+ * entry point gives each of `splits` CTAs per (batch, K / V head, key block)
+ * H / Hkv / splits of the group's query heads; each writes its share of dK,
+ * dV in fp32 to dkv_part, laid out [2][splits][B, Hkv, N, d] (dK shares,
+ * then dV shares; caller-allocated, 16-byte aligned, 2 * splits * B * Hkv *
+ * N * d floats), and a final pass sums the shares in split order and rounds
+ * them to dk, dv (deterministic).  splits must divide H / Hkv; splits = 1 is
+ * attn_bwd_gqa.  Dense layout; other arguments as for attn_bwd_gqa.
+ * attn_gqa_split_hint returns the smallest split count whose heaviest CTA
+ * does no more query-block iterations than the average SM (at most H / Hkv),
+ * for the current device.
+ */
+int attn_bwd_gqa_split(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                       void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
+                       int d, int causal, float scale, void* stream);
+int attn_bwd_gqa_split_f16(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                           void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
+                           int d, int causal, float scale, void* stream);
+int attn_gqa_split_hint(int B, int H, int Hkv, int N, int causal);
+
+/*
  * Packed variable-length batches, following the sj-techlog page ("2. module
  * 경계는 ..."): only the valid tokens are passed, concatenated, with
  * cu_seqlens (the cumulative token offset of each sequence) and the maximum

@@ -122,6 +122,12 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = [P, P, P, P, P, P, P, P, P, P, F, U64, U32, I, I, I, I, I, F, P]
                 fn.restype = I
+            for name in ("attn_bwd_gqa_split", "attn_bwd_gqa_split_f16"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+                fn.restype = I
+            L.attn_gqa_split_hint.argtypes = [I, I, I, I, I]
+            L.attn_gqa_split_hint.restype = I
             L.attn_status_string.argtypes = [I]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [P]
@@ -290,13 +296,15 @@ def forward(q, k, v, causal: bool = False, scale=None, o=None, lse=None, stream=
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=None, dv=None,
-             D=None, dq_accum=None, stream=None, o32=None):
+             D=None, dq_accum=None, stream=None, o32=None, splits=None):
     """dQ, dK, dV for [B,H,N,d] CUDA tensors (workspace allocated by torch if not given).
 
     With ``o32`` (the fp32 O of the training forward) D comes from
     rowsum(dO o O); otherwise the preprocess recomputes it from q, k, v, dO
     and lse.  ``o`` (the 16-bit forward output) is not read and may be None.
-    With grouped K / V heads, dk and dv are [B,Hkv,N,d], summed over each group.
+    With grouped K / V heads, dk and dv are [B,Hkv,N,d], summed over each group;
+    ``splits`` query-head shares per group run on separate CTAs (default: the
+    library's hint for this device and shape).
     """
     torch = _torch()
     (B, H, Hkv, N, d), f16 = _check_grouped(q, k, v, dO)
@@ -315,6 +323,17 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale=None, dq=None, dk=
         attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(),
                             lse.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), B, H, N, d,
                             causal, scale, s, f16, Hkv)
+    if splits is None:
+        splits = int(lib().attn_gqa_split_hint(B, H, Hkv, N, int(bool(causal)))) if Hkv != H else 1
+    if splits > 1:
+        # grouped heads split over CTAs: fp32 shares of dK, dV, summed at the end
+        part = torch.empty((2, splits, B, Hkv, N, d), dtype=torch.float32, device=q.device)
+        fn = lib().attn_bwd_gqa_split_f16 if f16 else lib().attn_bwd_gqa_split
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                  D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                  part.data_ptr(), splits, B, H, Hkv, N, d, int(bool(causal)), scale, s),
+               "attn_bwd_gqa_split")
+        return dq, dk, dv
     attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
              B, H, N, d, causal, scale, s, f16, Hkv)

@@ -279,12 +279,17 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
              int N, int d, int causal, float scale, void* stream, bool bf16,
              const void* block_mask = nullptr, long long mask_stride = 0,
              float* dk32 = nullptr, float* dv32 = nullptr, int acc32 = 0,
-             const DropoutArgs* drop = nullptr) {
+             const DropoutArgs* drop = nullptr, int splits = 1, float* split_part = nullptr) {
     // with fp32 gradient outputs (dk32, dv32) the 16-bit dk, dv are not used
     const bool f32 = dk32 != nullptr || dv32 != nullptr;
     if (f32 && (!dk32 || !dv32)) return ATTN_ERR_INVALID_ARG;
     if (f32 && !aligned16(dv32)) return ATTN_ERR_MISALIGNED;
     if (f32) dk = dv = dk32;
+    // group split: shares in split_part, summed into the 16-bit dk, dv at the end
+    if (splits < 1 || (splits > 1 && (f32 || !split_part || Hkv < 1 || H % Hkv != 0 ||
+                                      (H / Hkv) % splits != 0)))
+        return ATTN_ERR_INVALID_ARG;
+    if (splits > 1 && !aligned16(split_part)) return ATTN_ERR_MISALIGNED;
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d);
@@ -305,7 +310,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
         return rc;
     CUtensorMap tdq, tdk, tdv;
     if ((rc = make_map_f32(&tdq, dq_accum, BH, N, d))) return rc;
-    if (f32) {
+    if (f32 || splits > 1) {
         tdk = tdv = tq;   // not used: the fp32 rows are written directly
     } else if ((rc = make_map(&tdk, dk, BHkv, N, d, bf16)) || (rc = make_map(&tdv, dv, BHkv, N, d, bf16))) {
         return rc;
@@ -333,6 +338,13 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     a.dv32 = dv32;
     a.acc32 = acc32;
     if (drop != nullptr) a.drop = *drop;
+    const long long kv_elems = static_cast<long long>(BHkv) * N * d;
+    a.splits = splits;
+    if (splits > 1) {
+        a.dk32 = split_part;
+        a.dv32 = split_part + splits * kv_elems;
+        a.split_stride = kv_elems;
+    }
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
@@ -344,7 +356,13 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const 
     c.dq = dq;
     c.elems = static_cast<long long>(BH) * N * d;
     c.scale = scale;
-    return map_launch(launch_dq_convert(c, bf16, st));
+    if ((rc = map_launch(launch_dq_convert(c, bf16, st)))) return rc;
+    if (splits > 1) {
+        SplitSumArgs sk{a.dk32, dk, kv_elems, splits}, sv{a.dv32, dv, kv_elems, splits};
+        if ((rc = map_launch(launch_split_sum(sk, bf16, st)))) return rc;
+        if ((rc = map_launch(launch_split_sum(sv, bf16, st)))) return rc;
+    }
+    return ATTN_OK;
 }
 
 // Tensor maps over a packed variable-length [total, Hh, d] array (the valid
@@ -890,6 +908,34 @@ int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void
     if (rc) return rc;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
                     stream, false, nullptr, 0, nullptr, nullptr, 0, &dr);
+}
+
+int attn_gqa_split_hint(int B, int H, int Hkv, int N, int causal) {
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || N < 1) return 1;
+    const int G = H / Hkv;
+    const double nb = static_cast<double>((N + kTile - 1) / kTile);
+    // query-block iterations of the whole launch and of the heaviest CTA
+    const double total = static_cast<double>(B) * H * (causal ? nb * (nb + 1) / 2 : nb * nb);
+    const double per_sm = total / device_sm_count();
+    for (int s = 1; s <= G; ++s)
+        if (G % s == 0 && (G / s) * nb <= per_sm) return s;
+    return G;
+}
+
+int attn_bwd_gqa_split(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                       void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
+                       int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                    stream, true, nullptr, 0, nullptr, nullptr, 0, nullptr, splits, dkv_part);
+}
+
+int attn_bwd_gqa_split_f16(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                           void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
+                           int d, int causal, float scale, void* stream) {
+    return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                    stream, false, nullptr, 0, nullptr, nullptr, 0, nullptr, splits, dkv_part);
 }
 
 int attn_convert(const float* x, void* y, long long elems, float scale, void* stream) {

@@ -470,6 +470,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else {
         bkv = blockIdx.x;
         j = grid_block();
+        if (args.splits > 1) bkv /= args.splits;                 // x = (K / V head, split)
         if (args.cu_seqlens != nullptr) {
             j = blockIdx.x;
             bkv = grid_block();
@@ -484,12 +485,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Otherwise (dense, Hkv = H) the one query head of the same index, without
     // the divisions.  TMA head coordinates: kvc for K, V, dK, dV and qhead(it)
     // for Q, dO, dQ; qflat(it) is the (batch, head) index of the lse / D rows.
-    int N = args.N, tok0 = 0, kvc = bkv, qc0 = bkv, qf0 = bkv, group = 1;
+    int N = args.N, tok0 = 0, kvc = bkv, qc0 = bkv, qf0 = bkv, group = 1, split = 0;
     bool varlen = false;
     if constexpr (GENERAL) {
         const int b = bkv / args.Hkv, kvh = bkv % args.Hkv;
         group = args.H / args.Hkv;
         qf0 = b * args.H + kvh * group;
+        if (args.splits > 1) {
+            // this CTA's share of the group: query heads [split * group', (split + 1) * group')
+            split = static_cast<int>(blockIdx.x) - bkv * args.splits;
+            group /= args.splits;
+            qf0 += split * group;
+        }
         qc0 = qf0;
         if (args.cu_seqlens != nullptr) {
             varlen = true;
@@ -975,7 +982,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tmem_ld_sync(tmem + lane_off + col + cc, a32);
                         if (f32out) {
                             if (key_ok) {
-                                float* frow = (c == 0 ? args.dv32 : args.dk32) +
+                                float* frow = (c == 0 ? args.dv32 : args.dk32) + split * args.split_stride +
                                               (static_cast<size_t>(kvc) * N + j * kTile + r) * D + cc;
         #pragma unroll
                                 for (int v4 = 0; v4 < 8; ++v4) {
@@ -1081,7 +1088,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     // packed batch: x = key block, y / z = (sequence, K / V head)
     const dim3 grid = !GENERAL ? group_grid(a.num_kvblocks, BH, a.head_group > 0 ? a.head_group : BH)
                       : a.cu_seqlens != nullptr ? head_major_grid(a.num_kvblocks, BH)
-                                                : lpt_grid(a.num_kvblocks, BH);
+                                                : lpt_grid(a.num_kvblocks, BH * (a.splits > 1 ? a.splits : 1));
     kern<<<grid, C::THREADS, smem, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
     return cudaGetLastError();
 }
@@ -1123,7 +1130,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        bool bf16, cudaStream_t stream) {
     // the dense MHA kernel's head-group grid holds at most 65,535 key blocks
     const bool general = a.Hkv != a.H || a.cu_seqlens != nullptr || a.num_kvblocks > kMaxGridY ||
-                         a.dk32 != nullptr;
+                         a.dk32 != nullptr || a.splits > 1;
+    if (a.splits > 1 && (a.cu_seqlens != nullptr || a.dk32 == nullptr)) return cudaErrorInvalidValue;
     const bool sparse = a.block_mask != nullptr;   // dense layout, Hkv = H only
     const bool dropout = a.drop.drop_t > 0 && a.drop.drop_t < 256;   // dense layout, Hkv = H only
     if ((sparse || dropout) && general) return cudaErrorInvalidValue;

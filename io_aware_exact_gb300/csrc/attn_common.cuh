@@ -90,6 +90,11 @@ struct BwdArgs {
     float* dk32;
     float* dv32;
     int acc32;
+    // grouped heads, dense layout: the group's query heads are split over
+    // `splits` CTAs per (K / V head, key block); split s writes its share of
+    // dK, dV (fp32) at dk32 / dv32 + s * split_stride, summed afterwards
+    int splits;
+    long long split_stride;
     DropoutArgs drop;      // used by the dropout instantiations only
     float scale;           // softmax scale (tau)
     float scale_log2;      // tau * log2(e)
@@ -125,6 +130,13 @@ struct DqConvertArgs {
     float scale;            // tau
 };
 
+struct SplitSumArgs {
+    const float* part;      // [splits][elems] fp32 shares
+    void* out;              // [elems] 16-bit sum
+    long long elems;        // multiple of 8
+    int splits;
+};
+
 struct MergeArgs {
     float* o_acc;           // [rows, d] fp32 running output, merged in place
     float* lse_acc;         // [rows] running logsumexp, merged in place
@@ -149,6 +161,7 @@ cudaError_t launch_bwd_preprocess(const CUtensorMap& tq, const CUtensorMap& tk, 
 cudaError_t launch_bwd_preprocess_o32(const PreO32Args& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertArgs& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, bool bf16, cudaStream_t stream);
+cudaError_t launch_split_sum(const SplitSumArgs& a, bool bf16, cudaStream_t stream);
 
 
 // Grid layouts of the attention kernels.  Plain: x = (batch, head), y/z =

@@ -62,6 +62,25 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const MergeArgs a) {
     }
 }
 
+// out = sum over s of part[s], rounded to 16 bits; eight elements per step.
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_split_sum_kernel(const SplitSumArgs a) {
+    const long long n8 = a.elems / 8;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += stride) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+        for (int s = 0; s < a.splits; ++s) {
+            const float4* p = reinterpret_cast<const float4*>(a.part + s * a.elems) + 2 * i;
+            const float4 u = p[0], w = p[1];
+            x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
+            y.x += w.x; y.y += w.y; y.z += w.z; y.w += w.w;
+        }
+        reinterpret_cast<uint4*>(a.out)[i] = make_uint4(pack2<BF16>(x.x, x.y), pack2<BF16>(x.z, x.w),
+                                                        pack2<BF16>(y.x, y.y), pack2<BF16>(y.z, y.w));
+    }
+}
+
 static long long elementwise_blocks(long long work_items) {
     long long blocks = (work_items + 255) / 256;
     const long long cap = static_cast<long long>(device_sm_count()) * 8;
@@ -79,6 +98,13 @@ cudaError_t launch_merge(const MergeArgs& a, bool bf16, cudaStream_t stream) {
     ATTN_MERGE_CASE(128, false)
     return cudaErrorInvalidValue;
 #undef ATTN_MERGE_CASE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_sum(const SplitSumArgs& a, bool bf16, cudaStream_t stream) {
+    const long long blocks = elementwise_blocks(a.elems / 8);
+    if (bf16) attn_split_sum_kernel<true><<<blocks, 256, 0, stream>>>(a);
+    else attn_split_sum_kernel<false><<<blocks, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -255,3 +255,16 @@ def test_dropout_argument_errors(L):
     assert fwd(d=96) == 2
     assert bwd(dk=None) == 1
     assert bwd(dk=A + 2) == 3
+
+
+def test_group_split_argument_errors(L):
+    def split(part=A, splits=2, H=8, Hkv=2):
+        return L.attn_bwd_gqa_split(A, A, A, A, A, A, A, A, A, A, part, splits, 1, H, Hkv, 256, 64,
+                                    1, 0.125, None)
+
+    assert split() in (0, 4) and split(splits=4) in (0, 4) and split(splits=1) in (0, 4)
+    assert split(splits=3) == 1                 # 3 does not divide the group of 4
+    assert split(splits=0) == 1
+    assert split(part=None) == 1
+    assert split(part=A + 4) == 3
+    assert split(Hkv=3) == 1

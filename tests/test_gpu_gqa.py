@@ -29,7 +29,7 @@ def _grouped_inputs(B, H, Hkv, N, d, seed, dtype=torch.bfloat16):
     return {"q": xq["q"], "dO": xq["dO"], "k": xkv["k"], "v": xkv["v"]}
 
 
-def _run(x, causal, scale, path):
+def _run(x, causal, scale, path, splits=None):
     dev = torch.device("cuda:0")
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
     if path == "train":
@@ -38,7 +38,7 @@ def _run(x, causal, scale, path):
     else:
         o, lse = attn.forward(q, k, v, causal, scale)
         o32 = None
-    dq, dk, dv = attn.backward(q, k, v, o, lse, dO, causal, scale, o32=o32)
+    dq, dk, dv = attn.backward(q, k, v, o, lse, dO, causal, scale, o32=o32, splits=splits)
     torch.cuda.synchronize()
     assert attn.attn_get_device_status() == 0
     assert dk.shape == k.shape and dv.shape == v.shape
@@ -118,3 +118,25 @@ def test_grouped_argument_errors():
     rc = attn.lib().attn_fwd_gqa(q.data_ptr(), k.data_ptr(), k.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), 1, 3, 2, 128, 64, 1, 0.125, None)
     assert rc == 1
+
+
+@pytest.mark.parametrize("splits", [1, 2, 4])
+@pytest.mark.parametrize("causal", [True, False])
+def test_group_split_over_ctas(splits, causal):
+    """The group's query heads split over 1, 2 or 4 CTAs (fp32 shares of dK,
+    dV summed at the end) give the oracle's gradients; the shares are summed
+    in a fixed order, so dK, dV repeat bit for bit."""
+    x = _grouped_inputs(1, 8, 2, 640, 128, seed=77)
+    scale = 128 ** -0.5
+    out = _run(x, causal, scale, "train", splits=splits)
+    _compare(x, out, causal, scale)
+    again = _run(x, causal, scale, "train", splits=splits)
+    assert torch.equal(out["dk"], again["dk"]) and torch.equal(out["dv"], again["dv"])
+
+
+def test_group_split_hint():
+    L = attn.lib()
+    assert L.attn_gqa_split_hint(2, 16, 16, 8192, 1) == 1        # no groups
+    assert L.attn_gqa_split_hint(2, 16, 2, 8192, 1) == 2         # groups of 8 on 148 SMs
+    assert L.attn_gqa_split_hint(2, 16, 1, 8192, 1) == 4         # MQA
+    assert L.attn_gqa_split_hint(1, 4, 2, 256, 1) == 2           # tiny: all heads apart
