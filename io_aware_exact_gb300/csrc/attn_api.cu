@@ -174,10 +174,66 @@ int make_dropout(float p_drop, unsigned long long seed, unsigned int offset, Dro
     return ATTN_OK;
 }
 
+// Variants of the forward beyond the dense path (defaults: none).
+struct FwdOptions {
+    const void* block_mask = nullptr;   // block-sparse layout
+    long long mask_stride = 0;
+    const DropoutArgs* drop = nullptr;  // dropout on P
+};
+
+// Variants of the backward beyond the dense path (defaults: none).
+struct BwdOptions {
+    const void* block_mask = nullptr;   // block-sparse layout
+    long long mask_stride = 0;
+    float* dk32 = nullptr;              // fp32 dK, dV written (or added, acc32) instead of dk, dv
+    float* dv32 = nullptr;
+    int acc32 = 0;
+    const DropoutArgs* drop = nullptr;  // dropout on P
+    int splits = 1;                     // grouped heads: query-head shares per group
+    float* split_part = nullptr;        // their fp32 dK, dV shares
+};
+
+FwdOptions sparse_fwd(const void* mask, long long stride) {
+    FwdOptions o;
+    o.block_mask = mask;
+    o.mask_stride = stride;
+    return o;
+}
+
+BwdOptions sparse_bwd(const void* mask, long long stride) {
+    BwdOptions o;
+    o.block_mask = mask;
+    o.mask_stride = stride;
+    return o;
+}
+
+BwdOptions f32_bwd(float* dk32, float* dv32, int accumulate) {
+    BwdOptions o;
+    o.dk32 = dk32;
+    o.dv32 = dv32;
+    o.acc32 = accumulate;
+    return o;
+}
+
+BwdOptions drop_bwd(const DropoutArgs* drop) {
+    BwdOptions o;
+    o.drop = drop;
+    return o;
+}
+
+BwdOptions split_bwd(int splits, float* part) {
+    BwdOptions o;
+    o.splits = splits;
+    o.split_part = part;
+    return o;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse, int B,
              int H, int Hkv, int N, int d, int causal, float scale, void* stream, bool bf16,
-             const void* block_mask = nullptr, long long mask_stride = 0,
-             const DropoutArgs* drop = nullptr) {
+             const FwdOptions& opt = FwdOptions()) {
+    const void* block_mask = opt.block_mask;
+    const long long mask_stride = opt.mask_stride;
+    const DropoutArgs* drop = opt.drop;
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (o32 != nullptr && !aligned16(o32)) return ATTN_ERR_MISALIGNED;
     int rc = check_shape(B, H, N, d);
@@ -277,9 +333,15 @@ int pre_o32_impl(const float* o32, const void* dO, float* D, float* dq_accum, in
 int bwd_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
              const float* D, float* dq_accum, void* dq, void* dk, void* dv, int B, int H, int Hkv,
              int N, int d, int causal, float scale, void* stream, bool bf16,
-             const void* block_mask = nullptr, long long mask_stride = 0,
-             float* dk32 = nullptr, float* dv32 = nullptr, int acc32 = 0,
-             const DropoutArgs* drop = nullptr, int splits = 1, float* split_part = nullptr) {
+             const BwdOptions& opt = BwdOptions()) {
+    const void* block_mask = opt.block_mask;
+    const long long mask_stride = opt.mask_stride;
+    float* dk32 = opt.dk32;
+    float* dv32 = opt.dv32;
+    const int acc32 = opt.acc32;
+    const DropoutArgs* drop = opt.drop;
+    const int splits = opt.splits;
+    float* split_part = opt.split_part;
     // with fp32 gradient outputs (dk32, dv32) the 16-bit dk, dv are not used
     const bool f32 = dk32 != nullptr || dv32 != nullptr;
     if (f32 && (!dk32 || !dv32)) return ATTN_ERR_INVALID_ARG;
@@ -689,7 +751,7 @@ int attn_fwd_bsparse(const void* q, const void* k, const void* v, void* o, float
                      int d, int causal, float scale, void* stream) {
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, true,
-                    block_mask, mask_head_stride);
+                    sparse_fwd(block_mask, mask_head_stride));
 }
 
 int attn_fwd_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -697,7 +759,7 @@ int attn_fwd_bsparse_f16(const void* q, const void* k, const void* v, void* o, f
                          int d, int causal, float scale, void* stream) {
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, nullptr, lse, B, H, H, N, d, causal, scale, stream, false,
-                    block_mask, mask_head_stride);
+                    sparse_fwd(block_mask, mask_head_stride));
 }
 
 int attn_fwd_train_bsparse(const void* q, const void* k, const void* v, void* o, float* o32,
@@ -706,7 +768,7 @@ int attn_fwd_train_bsparse(const void* q, const void* k, const void* v, void* o,
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     if (!o32) return ATTN_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true,
-                    block_mask, mask_head_stride);
+                    sparse_fwd(block_mask, mask_head_stride));
 }
 
 int attn_fwd_train_bsparse_f16(const void* q, const void* k, const void* v, void* o, float* o32,
@@ -715,7 +777,7 @@ int attn_fwd_train_bsparse_f16(const void* q, const void* k, const void* v, void
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     if (!o32) return ATTN_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false,
-                    block_mask, mask_head_stride);
+                    sparse_fwd(block_mask, mask_head_stride));
 }
 
 int attn_bwd_bsparse(const void* q, const void* k, const void* v, const void* dO,
@@ -724,7 +786,7 @@ int attn_bwd_bsparse(const void* q, const void* k, const void* v, const void* dO
                      int N, int d, int causal, float scale, void* stream) {
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
-                    stream, true, block_mask, mask_head_stride);
+                    stream, true, sparse_bwd(block_mask, mask_head_stride));
 }
 
 int attn_bwd_bsparse_f16(const void* q, const void* k, const void* v, const void* dO,
@@ -733,7 +795,7 @@ int attn_bwd_bsparse_f16(const void* q, const void* k, const void* v, const void
                          int H, int N, int d, int causal, float scale, void* stream) {
     if (!block_mask) return ATTN_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
-                    stream, false, block_mask, mask_head_stride);
+                    stream, false, sparse_bwd(block_mask, mask_head_stride));
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -853,7 +915,7 @@ int attn_bwd_acc(const void* q, const void* k, const void* v, const void* dO, co
                  void* stream) {
     if (!dk32 || !dv32) return ATTN_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, nullptr, nullptr, B, H, Hkv, N, d, causal,
-                    scale, stream, true, nullptr, 0, dk32, dv32, accumulate != 0);
+                    scale, stream, true, f32_bwd(dk32, dv32, accumulate != 0));
 }
 
 int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO,
@@ -862,7 +924,7 @@ int attn_bwd_acc_f16(const void* q, const void* k, const void* v, const void* dO
                      int causal, float scale, void* stream) {
     if (!dk32 || !dv32) return ATTN_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, nullptr, nullptr, B, H, Hkv, N, d, causal,
-                    scale, stream, false, nullptr, 0, dk32, dv32, accumulate != 0);
+                    scale, stream, false, f32_bwd(dk32, dv32, accumulate != 0));
 }
 
 int attn_fwd_train_dropout(const void* q, const void* k, const void* v, void* o, float* o32,
@@ -872,8 +934,9 @@ int attn_fwd_train_dropout(const void* q, const void* k, const void* v, void* o,
     int rc = make_dropout(p_drop, seed, offset, &dr);
     if (rc) return rc;
     if (!o32) return ATTN_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true, nullptr, 0,
-                    &dr);
+    FwdOptions opt;
+    opt.drop = &dr;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, true, opt);
 }
 
 int attn_fwd_train_dropout_f16(const void* q, const void* k, const void* v, void* o, float* o32,
@@ -884,8 +947,9 @@ int attn_fwd_train_dropout_f16(const void* q, const void* k, const void* v, void
     int rc = make_dropout(p_drop, seed, offset, &dr);
     if (rc) return rc;
     if (!o32) return ATTN_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false, nullptr, 0,
-                    &dr);
+    FwdOptions opt;
+    opt.drop = &dr;
+    return fwd_impl(q, k, v, o, o32, lse, B, H, H, N, d, causal, scale, stream, false, opt);
 }
 
 int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* dO,
@@ -896,7 +960,7 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* dO
     int rc = make_dropout(p_drop, seed, offset, &dr);
     if (rc) return rc;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
-                    stream, true, nullptr, 0, nullptr, nullptr, 0, &dr);
+                    stream, true, drop_bwd(&dr));
 }
 
 int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void* dO,
@@ -907,7 +971,7 @@ int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void
     int rc = make_dropout(p_drop, seed, offset, &dr);
     if (rc) return rc;
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, H, N, d, causal, scale,
-                    stream, false, nullptr, 0, nullptr, nullptr, 0, &dr);
+                    stream, false, drop_bwd(&dr));
 }
 
 int attn_gqa_split_hint(int B, int H, int Hkv, int N, int causal) {
@@ -927,7 +991,7 @@ int attn_bwd_gqa_split(const void* q, const void* k, const void* v, const void* 
                        void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
                        int d, int causal, float scale, void* stream) {
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
-                    stream, true, nullptr, 0, nullptr, nullptr, 0, nullptr, splits, dkv_part);
+                    stream, true, split_bwd(splits, dkv_part));
 }
 
 int attn_bwd_gqa_split_f16(const void* q, const void* k, const void* v, const void* dO,
@@ -935,7 +999,7 @@ int attn_bwd_gqa_split_f16(const void* q, const void* k, const void* v, const vo
                            void* dv, float* dkv_part, int splits, int B, int H, int Hkv, int N,
                            int d, int causal, float scale, void* stream) {
     return bwd_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
-                    stream, false, nullptr, 0, nullptr, nullptr, 0, nullptr, splits, dkv_part);
+                    stream, false, split_bwd(splits, dkv_part));
 }
 
 int attn_convert(const float* x, void* y, long long elems, float scale, void* stream) {
