@@ -47,3 +47,22 @@ def test_single_process_helpers():
     import bench
     assert bench.dist_max(3.5) == 3.5
     assert bench.whole_job_rate(1, 50.0, 2.0) == pytest.approx(25000.0)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference (the fp64 oracle on the host cores) runs
+    without a GPU and prints one JSON line with the contract's keys."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["steps"] == 1
+    assert line["value"] > 0 and line["unit"] == "TFLOPS" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "fwdbwd_causal_peaked_b2_h16_n8192_d128"
