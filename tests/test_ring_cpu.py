@@ -26,17 +26,21 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 class OracleOps:
-    """Per-chunk arithmetic of the ring from the fp64 oracle (CPU tensors)."""
+    """Per-chunk arithmetic of the ring from the fp64 oracle (CPU tensors).
+    k, v may have fewer heads than q (grouped heads: query head h reads K / V
+    head oracle.kv_head_of(h, H, Hkv), and dK, dV sum over the group)."""
 
     def fwd_chunk(self, q, k, v, causal, scale):
         import oracle
         B, H, N, _ = q.shape
+        Hkv = k.shape[1]
         o = torch.empty((B, H, N, v.shape[-1]), dtype=torch.float64)
         lse = torch.empty((B, H, N), dtype=torch.float64)
         for b in range(B):
             for h in range(H):
-                ob, lb = oracle.attention_forward(q[b, h].numpy(), k[b, h].numpy(),
-                                                  v[b, h].numpy(), causal, scale)
+                g = oracle.kv_head_of(h, H, Hkv)
+                ob, lb = oracle.attention_forward(q[b, h].numpy(), k[b, g].numpy(),
+                                                  v[b, g].numpy(), causal, scale)
                 o[b, h], lse[b, h] = torch.from_numpy(ob), torch.from_numpy(lb)
         return o, lse
 
@@ -56,14 +60,17 @@ class OracleOps:
     def bwd_chunk(self, q, k, v, dO, lse, D, dq_acc, dk_acc, dv_acc, causal, scale):
         import oracle
         B, H = q.shape[:2]
-        dk, dv = torch.empty_like(k), torch.empty_like(v)
+        Hkv = k.shape[1]
+        dk, dv = torch.zeros_like(k), torch.zeros_like(v)
         for b in range(B):
             for h in range(H):
+                g = oracle.kv_head_of(h, H, Hkv)
                 gq, gk, gv = oracle.attention_backward_given_stats(
-                    q[b, h].numpy(), k[b, h].numpy(), v[b, h].numpy(), dO[b, h].numpy(),
+                    q[b, h].numpy(), k[b, g].numpy(), v[b, g].numpy(), dO[b, h].numpy(),
                     lse[b, h].numpy(), D[b, h].numpy(), causal, scale)
                 dq_acc[b, h] += torch.from_numpy(gq)
-                dk[b, h], dv[b, h] = torch.from_numpy(gk), torch.from_numpy(gv)
+                dk[b, g] += torch.from_numpy(gk)
+                dv[b, g] += torch.from_numpy(gv)
         if dk_acc is None:
             return dq_acc.clone(), dk, dv
         return dq_acc.clone(), dk_acc.add_(dk), dv_acc.add_(dv)
@@ -146,3 +153,27 @@ def test_ring_in_one_process_equals_whole_sequence(R, causal):
     got = {n: torch.cat(t, dim=2).numpy()
            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     _check(got, _reference(q.numpy(), k.numpy(), v.numpy(), dO.numpy(), causal, 0.8))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_with_grouped_heads_equals_whole_sequence(causal):
+    """Grouped K / V heads (4 query heads, 2 K / V heads) through the ring in
+    one process: K / V chunks of Hkv heads travel, dK, dV sum over each group."""
+    import oracle
+    from io_aware_exact_gb300 import ring
+    R, Nc, d = 3, 3, 4
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn((1, 4, R * Nc, d), generator=g, dtype=torch.float64)
+    dO = torch.randn((1, 4, R * Nc, d), generator=g, dtype=torch.float64)
+    k = torch.randn((1, 2, R * Nc, d), generator=g, dtype=torch.float64)
+    v = torch.randn((1, 2, R * Nc, d), generator=g, dtype=torch.float64)
+    qs, ks, vs, dOs = (_chunks(t, R) for t in (q, k, v, dO))
+    o, lse, o32 = ring.ring_forward(qs, ks, vs, causal, 0.7, OracleOps)
+    dq, dk, dv = ring.ring_backward(qs, ks, vs, o32, lse, dOs, causal, 0.7, OracleOps)
+    o_ref, lse_ref = oracle.attention_forward_grouped(q[0].numpy(), k[0].numpy(), v[0].numpy(),
+                                                      causal, 0.7)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward_grouped(
+        q[0].numpy(), k[0].numpy(), v[0].numpy(), dO[0].numpy(), causal, 0.7)
+    for got, ref in ((o, o_ref), (lse, lse_ref), (dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+        err = np.max(np.abs(torch.cat(got, dim=2)[0].numpy() - ref))
+        assert err < 1e-11
