@@ -54,6 +54,32 @@ def test_ring_equals_whole_sequence(R, N, d, causal, dtype):
             check_tensor(n, _f64(got[n][0, h]), ref)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_with_grouped_heads(causal):
+    """Grouped K / V heads (8 query heads, 2 K / V heads) through the CUDA ring:
+    the forward takes the grouped path, attn_bwd_acc sums each group's dK, dV
+    into the travelling fp32 sums."""
+    B, H, Hkv, N, d, R = 1, 8, 2, 768, 128, 3
+    scale = d ** -0.5
+    xq = make_inputs(B, H, N, d, seed=720)
+    xkv = make_inputs(B, Hkv, N, d, seed=721)
+    x = {"q": xq["q"], "dO": xq["dO"], "k": xkv["k"], "v": xkv["v"]}
+    dev = torch.device("cuda:0")
+    ch = {n: [c.contiguous() for c in torch.chunk(t.to(dev), R, dim=2)] for n, t in x.items()}
+    o, lse, o32 = ring.ring_forward(ch["q"], ch["k"], ch["v"], causal, scale)
+    dq, dk, dv = ring.ring_backward(ch["q"], ch["k"], ch["v"], o32, lse, ch["dO"], causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    got = {n: torch.cat(t, dim=2)[0] for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+    q, k, v, dO = (_f64(x[n][0]) for n in ("q", "k", "v", "dO"))
+    o_ref, lse_ref = oracle.attention_forward_grouped(q, k, v, causal, scale)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward_grouped(q, k, v, dO, causal, scale)
+    check_lse(torch.cat(lse, dim=2)[0].cpu().numpy().astype(np.float64).reshape(-1),
+              lse_ref.reshape(-1))
+    for n, ref in (("o", o_ref), ("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
+        check_tensor(n, _f64(got[n]).reshape(-1, d), ref.reshape(-1, d))
+
+
 def test_merge_kernel_matches_oracle_and_handles_empty_partials():
     dev = torch.device("cuda:0")
     g = torch.Generator().manual_seed(5)
