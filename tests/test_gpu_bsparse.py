@@ -78,6 +78,8 @@ def _compare(x, mask, out, causal, scale):
     (2, 2, 640, 128, True, 0.6, True, torch.float16),
     (1, 3, 1536, 64, True, 0.3, False, torch.bfloat16),
     (1, 2, 2048, 128, False, 0.25, False, torch.bfloat16),
+    (1, 1, 1, 64, False, 1.0, True, torch.bfloat16),          # one row, one tile
+    (2, 2, 200, 64, True, 0.7, True, torch.float16),          # ragged, fp16, d = 64
 ])
 def test_block_sparse_matches_oracle(B, H, N, d, causal, density, shared, dtype):
     x = make_inputs(B, H, N, d, seed=500 + N + d, dtype=dtype)

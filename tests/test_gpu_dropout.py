@@ -42,6 +42,9 @@ def _run(x, p, seed, offset, causal, scale):
     (1, 2, 1000, 128, True, 0.5, torch.bfloat16),
     (2, 1, 640, 128, False, 0.3, torch.float16),
     (1, 3, 384, 64, True, 0.2, torch.bfloat16),
+    (1, 1, 1, 128, True, 0.4, torch.bfloat16),      # one row
+    (1, 2, 129, 64, True, 0.05, torch.float16),     # ragged tail, fp16, d = 64
+    (1, 1, 300, 128, False, 3 / 512, torch.bfloat16),   # 256 (1 - p) = 254.5: ties round to even
 ])
 def test_dropout_matches_oracle(B, H, N, d, causal, p, dtype):
     scale = d ** -0.5

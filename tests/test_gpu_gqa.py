@@ -134,6 +134,12 @@ def test_group_split_over_ctas(splits, causal):
     assert torch.equal(out["dk"], again["dk"]) and torch.equal(out["dv"], again["dv"])
 
 
+def test_group_split_fp16_d64():
+    x = _grouped_inputs(2, 6, 2, 257, 64, seed=78, dtype=torch.float16)
+    out = _run(x, True, 64 ** -0.5, "train", splits=3)
+    _compare(x, out, True, 64 ** -0.5)
+
+
 def test_group_split_hint():
     L = attn.lib()
     assert L.attn_gqa_split_hint(2, 16, 16, 8192, 1) == 1        # no groups
