@@ -365,6 +365,9 @@ def run_ours(args):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
+        "step_ms_p10_p50_p90": [round(x, 4) for x in _percentiles(t_step)],
+        "seed": w.seed + 100 * rank,
+        "env": _environment(dev),
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
@@ -407,6 +410,29 @@ def profile_traffic(workload):
         return int(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+def _percentiles(xs, qs=(0.1, 0.5, 0.9)):
+    """Nearest-rank percentiles of a list of times."""
+    ys = sorted(xs)
+    return [ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))] for q in qs]
+
+
+def _environment(dev):
+    """Device, driver and library versions for the JSON line."""
+    import torch
+    import io_aware_exact_gb300 as attn
+    prop = torch.cuda.get_device_properties(dev)
+    env = {"gpu": prop.name, "sm_count": prop.multi_processor_count,
+           "cc": "%d.%d" % (prop.major, prop.minor), "torch": torch.__version__,
+           "cuda_runtime": torch.version.cuda, "library": attn.version()}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True, timeout=20)
+        env["driver"] = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        env["driver"] = None
+    return env
 
 
 def _oracle_step(w, x, heads):
