@@ -143,6 +143,6 @@ def test_group_split_fp16_d64():
 def test_group_split_hint():
     L = attn.lib()
     assert L.attn_gqa_split_hint(2, 16, 16, 8192, 1) == 1        # no groups
-    assert L.attn_gqa_split_hint(2, 16, 2, 8192, 1) == 2         # groups of 8 on 148 SMs
+    assert L.attn_gqa_split_hint(2, 16, 2, 8192, 1) == 2         # groups of 8 on 152 SMs
     assert L.attn_gqa_split_hint(2, 16, 1, 8192, 1) == 4         # MQA
     assert L.attn_gqa_split_hint(1, 4, 2, 256, 1) == 2           # tiny: all heads apart
