@@ -477,3 +477,26 @@ def attention_backward_dropout(q, k, v, dO, causal: bool, scale: float, keep, p_
     D = (p * dp).sum(axis=1)
     ds = p * (dp - D[:, None])
     return scale * (ds @ k), scale * (ds.T @ q), dv
+
+
+def attention_forward_offset(q, k, v, causal: bool, scale: float, offset: int):
+    """O, lse of one head whose nq queries attend to nk keys with the causal
+    mask shifted by ``offset``: key j is visible to query i iff
+    j <= i + offset.  offset = nk - nq aligns the last query with the last
+    key (bottom-right, e.g. a query chunk after nk - nq cached keys);
+    offset = 0 is the top-left mask of the rest of this module.  Rows with no
+    visible key give O = 0, lse = -inf (the block-sparse reading)."""
+    nq, nk = len(q), len(k)
+    vis = np.ones((nq, nk), bool)
+    if causal:
+        vis = np.arange(nk)[None, :] <= (np.arange(nq)[:, None] + offset)
+    return attention_forward_masked(q, k, v, vis, scale)
+
+
+def attention_backward_offset(q, k, v, dO, causal: bool, scale: float, offset: int):
+    """(dQ, dK, dV, lse, D) of attention_forward_offset."""
+    nq, nk = len(q), len(k)
+    vis = np.ones((nq, nk), bool)
+    if causal:
+        vis = np.arange(nk)[None, :] <= (np.arange(nq)[:, None] + offset)
+    return attention_backward_masked(q, k, v, dO, vis, scale)

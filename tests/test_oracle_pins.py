@@ -654,3 +654,50 @@ def test_dropout_backward_matches_finite_differences(causal):
                       (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
         scale = max(1.0, np.max(np.abs(want)))
         assert np.max(np.abs(got - want)) / scale < 1e-6
+
+
+# --------------------------------------------------------------------------
+# Queries and keys of different lengths (shifted causal mask)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("nq,nk", [(3, 8), (8, 8), (8, 5)])
+def test_offset_causal_rows_are_prefix_attention(nq, nk):
+    """Bottom-right alignment (offset = nk - nq): query i attends to keys
+    [0, i + nk - nq] exactly, each row equal to the C oracle over that key
+    prefix; rows with no key (nq > nk) are O = 0, lse = -inf.  With
+    offset = 0 and nq = nk it is the top-left causal mask."""
+    r = _rng(120 + nq + nk)
+    q, k, v = r.normal(size=(nq, 3)), r.normal(size=(nk, 3)), r.normal(size=(nk, 2))
+    off = nk - nq
+    o, lse = oracle.attention_forward_offset(q, k, v, True, 0.8, off)
+    for i in range(nq):
+        last = i + off
+        if last < 0:
+            assert np.all(o[i] == 0.0) and lse[i] == -np.inf
+            continue
+        oi, li = oracle.attention_forward(q[i:i + 1], k[:last + 1], v[:last + 1], False, 0.8)
+        assert np.max(np.abs(o[i] - oi[0])) < 1e-13 and abs(lse[i] - li[0]) < 1e-13
+    if nq <= nk:   # the last query sees every key
+        assert abs(lse[-1] - oracle.attention_forward(q[-1:], k, v, False, 0.8)[1][0]) < 1e-13
+    if nq == nk:
+        o0, l0 = oracle.attention_forward_offset(q, k, v, True, 0.8, 0)
+        o1, l1 = oracle.attention_forward(q, k, v, True, 0.8)
+        assert np.max(np.abs(o0 - o1)) < 1e-13 and np.max(np.abs(l0 - l1)) < 1e-13
+
+
+def test_offset_backward_matches_finite_differences():
+    r = _rng(130)
+    nq, nk, tau = 4, 7, 0.7
+    q, k = r.normal(size=(nq, 3)), r.normal(size=(nk, 3))
+    v, dO = r.normal(size=(nk, 2)), r.normal(size=(nq, 2))
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward_offset(qq, kk, vv, True, tau, nk - nq)
+        return float(np.sum(o * dO))
+
+    dq, dk, dv, _, _ = oracle.attention_backward_offset(q, k, v, dO, True, tau, nk - nq)
+    for got, want in ((dq, _fd_grad(q, lambda x: loss(x, k, v))),
+                      (dk, _fd_grad(k, lambda x: loss(q, x, v))),
+                      (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
