@@ -268,3 +268,30 @@ def test_group_split_argument_errors(L):
     assert split(part=None) == 1
     assert split(part=A + 4) == 3
     assert split(Hkv=3) == 1
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(L, tmp_path):
+    """include/attn.h compiles as C99 with warnings as errors, and a C program
+    links against the library and calls it (no device work: an argument error
+    is reported on the host)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "attn.h"\n'
+        "int main(void) {\n"
+        '    printf("%s|%s\\n", attn_version(), attn_status_string(ATTN_ERR_TIMEOUT));\n'
+        "    return attn_fwd(0, 0, 0, 0, 0, 1, 1, 128, 64, 0, 0.125f, 0) == ATTN_ERR_INVALID_ARG"
+        " ? 0 : 1;\n}\n")
+    libdir = os.path.dirname(attn.LIB_PATH)
+    exe = tmp_path / "abi"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lattn_gb300",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("io_aware_exact_gb300") and "bounded wait" in r.stdout
