@@ -134,7 +134,10 @@ def lib():
             L.attn_get_device_status.restype = I
             L.attn_selftest_timeout.argtypes = [I, P]
             L.attn_selftest_timeout.restype = I
+            L.attn_version.argtypes = []
             L.attn_version.restype = ctypes.c_char_p
+            L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+            L.attn_bwd_noalloc.restype = I
             _lib = L
     return _lib
 

@@ -6,6 +6,7 @@ declares and that argument errors are reported synchronously with the
 documented codes, before any device work.
 """
 import ast
+import ctypes
 import re
 import glob
 import os
@@ -295,3 +296,12 @@ def test_header_is_plain_c_and_the_library_links_from_c(L, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("io_aware_exact_gb300") and "bounded wait" in r.stdout
+
+
+def test_binding_declares_every_entry_point(L):
+    """Every function of include/attn.h has ctypes argument and result types in
+    the binding, so no pointer or 64-bit argument is passed as a C int."""
+    for n in attn.header_functions():
+        f = getattr(L, n)
+        assert f.argtypes is not None, n
+        assert f.restype in (ctypes.c_int, ctypes.c_char_p), n
