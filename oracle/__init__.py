@@ -4,10 +4,13 @@ Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
 ``cpu_baseline`` / reference leg may import this package.  It shares no code
 with the CUDA library in ``io_aware_exact_gb300``.  The dense functions'
 arithmetic lives in ``attn_oracle.c`` (plain C, fp64), built by :func:`build`
-with the host compiler, and this module only marshals numpy arrays into it;
-the functions with an explicit visibility mask (block-sparse layouts) are
-written here with numpy fp64 matrix products, the same definitions with
-dropped scores excluded from the softmax.
+with the host compiler, and this module only marshals numpy arrays into it.
+Written here with numpy fp64 instead: the functions with an explicit
+visibility mask (block-sparse layouts, a shifted causal mask for unequal
+lengths), the exact merge of partial results and the backward with given
+row statistics (chunked / ring attention), and dropout (Philox4x32-10, the
+keep mask and dropout attention); grouped heads and packed batches compose
+the single-head functions.
 
 The functions follow, one head at a time:
 
