@@ -16,7 +16,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import check_lse, check_tensor
+from parity import Parity
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,7 @@ def test_dropout_matches_oracle(B, H, N, d, causal, p, dtype):
     x = make_inputs(B, H, N, d, seed=800 + N + d, dtype=dtype)
     offset = 17
     out = _run(x, p, SEED, offset, causal, scale)
+    pc = Parity("dropout p=%g" % p)
     for b in range(B):
         for h in range(H):
             bh = b * H + h
@@ -59,10 +60,11 @@ def test_dropout_matches_oracle(B, H, N, d, causal, p, dtype):
             o_ref, lse_ref = oracle.attention_forward_dropout(q, k, v, causal, scale, keep, p)
             dq_ref, dk_ref, dv_ref = oracle.attention_backward_dropout(q, k, v, dO, causal, scale,
                                                                        keep, p)
-            check_lse(out["lse"][b, h].numpy().astype(np.float64), lse_ref)
+            pc.add_lse(out["lse"][b, h].numpy().astype(np.float64), lse_ref)
             for n, ref in (("o", o_ref), ("o32", o_ref), ("dq", dq_ref), ("dk", dk_ref),
                            ("dv", dv_ref)):
-                check_tensor(n, _f64(out[n][b, h]), ref)
+                pc.add(n, _f64(out[n][b, h]), ref)
+    pc.check()
 
 
 def test_dropout_zero_is_the_plain_training_path():

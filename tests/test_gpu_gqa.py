@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import check_lse, check_tensor
+from parity import Parity, check_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -47,17 +47,19 @@ def _run(x, causal, scale, path, splits=None):
 
 def _compare(x, out, causal, scale):
     B = x["q"].shape[0]
+    pc = Parity("grouped")
     for b in range(B):
         q, k, v, dO = (_f64(x[n][b]) for n in ("q", "k", "v", "dO"))
         o_ref, lse_ref = oracle.attention_forward_grouped(q, k, v, causal, scale)
         dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward_grouped(q, k, v, dO, causal, scale)
         for h in range(q.shape[0]):
-            check_tensor("O", _f64(out["o"][b, h]), o_ref[h])
-            check_lse(out["lse"][b, h].numpy().astype(np.float64), lse_ref[h])
-            check_tensor("dQ", _f64(out["dq"][b, h]), dq_ref[h])
+            pc.add("O", _f64(out["o"][b, h]), o_ref[h])
+            pc.add_lse(out["lse"][b, h].numpy().astype(np.float64), lse_ref[h])
+            pc.add("dQ", _f64(out["dq"][b, h]), dq_ref[h])
         for g in range(k.shape[0]):
-            check_tensor("dK", _f64(out["dk"][b, g]), dk_ref[g])
-            check_tensor("dV", _f64(out["dv"][b, g]), dv_ref[g])
+            pc.add("dK", _f64(out["dk"][b, g]), dk_ref[g])
+            pc.add("dV", _f64(out["dv"][b, g]), dv_ref[g])
+    pc.check()
 
 
 CASES = [

@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import WORKLOADS, make_inputs
-from parity import check_lse, check_tensor, sample_rows
+from parity import Parity, check_tensor, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -47,30 +47,42 @@ def _run_gpu(x, causal, scale, backward, f16=False, path="train"):
     return {kk: vv.cpu() for kk, vv in out.items()}
 
 
-def _compare_head(x, out, b, h, causal, scale, backward, rows=None, cols=None, report=None):
+def _compare_head(x, out, b, h, causal, scale, backward, pc, rows=None, cols=None):
+    """Add head (b, h)'s outputs and the oracle's to the collector pc."""
     q, k, v = (_f64(x[n][b, h]) for n in ("q", "k", "v"))
-    N = q.shape[0]
     o_ref, lse_ref = oracle.attention_forward(q, k, v, causal, scale, rows=rows)
     sel = slice(None) if rows is None else rows
-    check_tensor("O", _f64(out["o"][b, h])[sel], o_ref, report)
-    check_lse(out["lse"][b, h].numpy().astype(np.float64)[sel], lse_ref, report)
+    pc.add("O", _f64(out["o"][b, h])[sel], o_ref)
+    pc.add_lse(out["lse"][b, h].numpy().astype(np.float64)[sel], lse_ref)
     if not backward:
         return
     dO = _f64(x["dO"][b, h])
     if rows is None and cols is None:
         dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward(q, k, v, dO, causal, scale)
-        check_tensor("dQ", _f64(out["dq"][b, h]), dq_ref, report)
-        check_tensor("dK", _f64(out["dk"][b, h]), dk_ref, report)
-        check_tensor("dV", _f64(out["dv"][b, h]), dv_ref, report)
+        pc.add("dQ", _f64(out["dq"][b, h]), dq_ref)
+        pc.add("dK", _f64(out["dk"][b, h]), dk_ref)
+        pc.add("dV", _f64(out["dv"][b, h]), dv_ref)
         return
     _, _, dq_ref = oracle.attention_backward_rows(q, k, v, dO, causal, scale, rows=rows)
-    check_tensor("dQ", _f64(out["dq"][b, h])[rows], dq_ref, report)
+    pc.add("dQ", _f64(out["dq"][b, h])[rows], dq_ref)
     lse_all, D_all, _ = oracle.attention_backward_rows(q, k, v, dO, causal, scale,
                                                        with_dq=False)
     dk_ref, dv_ref = oracle.attention_backward_cols(q, k, v, dO, lse_all, D_all, causal, scale,
                                                     cols=cols)
-    check_tensor("dK", _f64(out["dk"][b, h])[cols], dk_ref, report)
-    check_tensor("dV", _f64(out["dv"][b, h])[cols], dv_ref, report)
+    pc.add("dK", _f64(out["dk"][b, h])[cols], dk_ref)
+    pc.add("dV", _f64(out["dv"][b, h])[cols], dv_ref)
+
+
+def _compare_heads(x, out, heads, causal, scale, backward, label, rows=None, cols=None):
+    """Compare the listed heads; each tensor is judged over all of them at once."""
+    pc = Parity(label)
+    for (b, h) in heads:
+        _compare_head(x, out, b, h, causal, scale, backward, pc, rows=rows, cols=cols)
+    pc.check()
+
+
+def _all_heads(B, H):
+    return [(b, h) for b in range(B) for h in range(H)]
 
 
 SMALL = [
@@ -95,9 +107,7 @@ SMALL = [
 def test_forward_small(B, H, N, d, causal):
     x = make_inputs(B, H, N, d, seed=7 + N + d, with_grad=False)
     out = _run_gpu(x, causal, d ** -0.5, backward=False)
-    for b in range(B):
-        for h in range(H):
-            _compare_head(x, out, b, h, causal, d ** -0.5, backward=False)
+    _compare_heads(x, out, _all_heads(B, H), causal, d ** -0.5, False, "B%d H%d N%d d%d" % (B, H, N, d))
 
 
 @pytest.mark.parametrize("path", ["train", "exact"])
@@ -105,9 +115,7 @@ def test_forward_small(B, H, N, d, causal):
 def test_backward_small(B, H, N, d, causal, path):
     x = make_inputs(B, H, N, d, seed=11 + N + d)
     out = _run_gpu(x, causal, d ** -0.5, backward=True, path=path)
-    for b in range(B):
-        for h in range(H):
-            _compare_head(x, out, b, h, causal, d ** -0.5, backward=True)
+    _compare_heads(x, out, _all_heads(B, H), causal, d ** -0.5, True, "B%d H%d N%d d%d" % (B, H, N, d))
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -115,15 +123,13 @@ def test_scale_not_inverse_sqrt_d(causal):
     """A scale other than 1/sqrt(d) must enter both S and the gradients."""
     x = make_inputs(1, 2, 300, 64, seed=5)
     out = _run_gpu(x, causal, 0.3, backward=True)
-    for h in range(2):
-        _compare_head(x, out, 0, h, causal, 0.3, backward=True)
+    _compare_heads(x, out, _all_heads(1, 2), causal, 0.3, True, "scale 0.3")
 
 
 def test_fp16_entry_points():
     x = make_inputs(1, 2, 320, 128, seed=9, dtype=torch.float16)
     out = _run_gpu(x, True, 128 ** -0.5, backward=True)
-    for h in range(2):
-        _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
+    _compare_heads(x, out, _all_heads(1, 2), True, 128 ** -0.5, True, "fp16")
 
 
 @pytest.mark.parametrize("path", ["train", "exact"])
@@ -132,8 +138,7 @@ def test_peaked_rows(path):
     and the cancellation in dS = P (dP - D)."""
     x = make_inputs(1, 2, 1024, 128, seed=13, qk_mult=8.0)
     out = _run_gpu(x, True, 128 ** -0.5, backward=True, path=path)
-    for h in range(2):
-        _compare_head(x, out, 0, h, True, 128 ** -0.5, backward=True)
+    _compare_heads(x, out, _all_heads(1, 2), True, 128 ** -0.5, True, "Q, K x8")
 
 
 # ---------------------------------------------------------------------------
@@ -159,8 +164,7 @@ def test_workload(name, nheads):
     w = WORKLOADS[name]
     x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_grad=w.backward)
     out = _run_gpu(x, w.causal, w.scale, backward=w.backward)
-    for (b, h) in _heads(w, nheads, w.seed):
-        _compare_head(x, out, b, h, w.causal, w.scale, w.backward)
+    _compare_heads(x, out, _heads(w, nheads, w.seed), w.causal, w.scale, w.backward, name)
 
 
 def test_workload_peaked_exact_preprocess():
@@ -168,8 +172,7 @@ def test_workload_peaked_exact_preprocess():
     w = WORKLOADS["fwdbwd_causal_peaked_b2_h16_n8192_d128"]
     x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
     out = _run_gpu(x, w.causal, w.scale, backward=True, path="exact")
-    for (b, h) in _heads(w, 2, w.seed + 1):
-        _compare_head(x, out, b, h, w.causal, w.scale, True)
+    _compare_heads(x, out, _heads(w, 2, w.seed + 1), w.causal, w.scale, True, "exact D")
 
 
 def test_autograd_function():
@@ -181,14 +184,16 @@ def test_autograd_function():
     o.backward(x["dO"].to(dev))
     out = {"o": o.detach().cpu(), "dq": q.grad.cpu(), "dk": k.grad.cpu(), "dv": v.grad.cpu(),
            "lse": torch.zeros(1, 2, 300)}
+    pc = Parity("autograd")
     for h in range(2):
         qh, kh, vh, dOh = (_f64(x[n][0, h]) for n in ("q", "k", "v", "dO"))
         o_ref, _ = oracle.attention_forward(qh, kh, vh, True, 64 ** -0.5)
-        check_tensor("O", _f64(out["o"][0, h]), o_ref)
+        pc.add("O", _f64(out["o"][0, h]), o_ref)
         dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward(qh, kh, vh, dOh, True, 64 ** -0.5)
-        check_tensor("dQ", _f64(out["dq"][0, h]), dq_ref)
-        check_tensor("dK", _f64(out["dk"][0, h]), dk_ref)
-        check_tensor("dV", _f64(out["dv"][0, h]), dv_ref)
+        pc.add("dQ", _f64(out["dq"][0, h]), dq_ref)
+        pc.add("dK", _f64(out["dk"][0, h]), dk_ref)
+        pc.add("dV", _f64(out["dv"][0, h]), dv_ref)
+    pc.check()
 
 
 def test_workload_long_sequence():
@@ -198,7 +203,8 @@ def test_workload_long_sequence():
     out = _run_gpu(x, w.causal, w.scale, backward=True)
     rows = sample_rows(w.N, 96, seed=1)
     cols = sample_rows(w.N, 96, seed=2)
-    _compare_head(x, out, 0, w.H - 1, w.causal, w.scale, True, rows=rows, cols=cols)
+    _compare_heads(x, out, [(0, w.H - 1)], w.causal, w.scale, True, "N=32768 sampled",
+                   rows=rows, cols=cols)
 
 
 def test_no_nxn_buffer_long_sequence():
@@ -231,7 +237,7 @@ def test_timeout_path_reports_and_context_survives():
     assert attn.attn_get_device_status() == 0
     x = make_inputs(1, 1, 128, 64, seed=3, with_grad=False)
     out = _run_gpu(x, False, 0.125, backward=False)
-    _compare_head(x, out, 0, 0, False, 0.125, backward=False)
+    _compare_heads(x, out, [(0, 0)], False, 0.125, False, "after timeout")
 
 
 def test_repeated_calls_are_stable():

@@ -17,7 +17,7 @@ import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300 import ring
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import check_lse, check_tensor
+from parity import Parity, check_lse, check_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -45,13 +45,15 @@ def test_ring_equals_whole_sequence(R, N, d, causal, dtype):
     assert attn.attn_get_device_status() == 0
     got = {n: torch.cat(t, dim=2) for n, t in
            (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    pc = Parity("ring R=%d" % R)
     for h in range(H):
         q, k, v, dO = (_f64(x[n][0, h]) for n in ("q", "k", "v", "dO"))
         o_ref, lse_ref = oracle.attention_forward(q, k, v, causal, scale)
         dq_ref, dk_ref, dv_ref, _, _ = oracle.attention_backward(q, k, v, dO, causal, scale)
-        check_lse(got["lse"][0, h].cpu().numpy().astype(np.float64), lse_ref)
+        pc.add_lse(got["lse"][0, h].cpu().numpy().astype(np.float64), lse_ref)
         for n, ref in (("o", o_ref), ("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
-            check_tensor(n, _f64(got[n][0, h]), ref)
+            pc.add(n, _f64(got[n][0, h]), ref)
+    pc.check()
 
 
 @pytest.mark.parametrize("causal", [True, False])

@@ -15,7 +15,7 @@ torch = pytest.importorskip("torch")
 
 import oracle
 import io_aware_exact_gb300 as attn
-from parity import check_lse, check_tensor
+from parity import Parity, check_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -54,18 +54,20 @@ def _compare(x, cu, max_s, out, causal, scale):
     o_ref, lse_ref = oracle.attention_forward_varlen(q, k, v, cu, max_s, causal, scale)
     dq_ref, dk_ref, dv_ref = oracle.attention_backward_varlen(q, k, v, dO, cu, causal, scale)
     lse = out["lse"].numpy().astype(np.float64)
+    pc = Parity("varlen")
     for b in range(len(cu) - 1):
         s0, s1 = int(cu[b]), int(cu[b + 1])
         assert np.all(lse[b, :, s1 - s0:] == SENTINEL), "lse past the sequence was written"
         if s1 == s0:
             continue
         for h in range(q.shape[1]):
-            check_tensor("O", _f64(out["o"][s0:s1, h]), o_ref[s0:s1, h])
-            check_lse(lse[b, h, :s1 - s0], lse_ref[b, h, :s1 - s0])
-            check_tensor("dQ", _f64(out["dq"][s0:s1, h]), dq_ref[s0:s1, h])
+            pc.add("O", _f64(out["o"][s0:s1, h]), o_ref[s0:s1, h])
+            pc.add_lse(lse[b, h, :s1 - s0], lse_ref[b, h, :s1 - s0])
+            pc.add("dQ", _f64(out["dq"][s0:s1, h]), dq_ref[s0:s1, h])
         for g in range(k.shape[1]):
-            check_tensor("dK", _f64(out["dk"][s0:s1, g]), dk_ref[s0:s1, g])
-            check_tensor("dV", _f64(out["dv"][s0:s1, g]), dv_ref[s0:s1, g])
+            pc.add("dK", _f64(out["dk"][s0:s1, g]), dk_ref[s0:s1, g])
+            pc.add("dV", _f64(out["dv"][s0:s1, g]), dv_ref[s0:s1, g])
+    pc.check()
 
 
 CASES = [

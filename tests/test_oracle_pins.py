@@ -656,6 +656,65 @@ def test_dropout_backward_matches_finite_differences(causal):
         assert np.max(np.abs(got - want)) / scale < 1e-6
 
 
+def _dropout_mask_average(p, n, d, masks, causal, seed_base):
+    """Per-mask outputs of the dropout functions over `masks` generator seeds
+    (same inputs), with the undropped results: returns (samples, plain),
+    samples[name] of shape [masks, ...]."""
+    r = _rng(140 + int(causal))
+    tau = 0.5
+    q, k = r.normal(size=(n, d)), r.normal(size=(n, d))
+    v, dO = r.normal(size=(n, d)), r.normal(size=(n, d))
+    ones = np.ones((n, 1))
+    samples = {"O": [], "O1": [], "dQ": [], "dK": [], "dV": [], "dV1": []}
+    for m in range(masks):
+        keep = oracle.dropout_keep(m % 7, n, n, p, seed_base + m, 3)
+        samples["O"].append(oracle.attention_forward_dropout(q, k, v, causal, tau, keep, p)[0])
+        samples["O1"].append(oracle.attention_forward_dropout(q, k, ones, causal, tau, keep, p)[0])
+        dq, dk, dv = oracle.attention_backward_dropout(q, k, v, dO, causal, tau, keep, p)
+        samples["dQ"].append(dq)
+        samples["dK"].append(dk)
+        samples["dV"].append(dv)
+        samples["dV1"].append(oracle.attention_backward_dropout(q, k, ones, ones, causal, tau, keep, p)[2])
+    samples = {kk: np.stack(vv) for kk, vv in samples.items()}
+    o, _ = oracle.attention_forward(q, k, v, causal, tau)
+    dq, dk, dv, _, _ = oracle.attention_backward(q, k, v, dO, causal, tau)
+    dv1 = oracle.attention_backward(q, k, ones, ones, causal, tau)[2]
+    return samples, {"O": o, "O1": np.ones((n, 1)), "dQ": dq, "dK": dk, "dV": dv, "dV1": dv1}
+
+
+@pytest.mark.parametrize("p,causal,masks", [(0.99, False, 480), (0.3, True, 240)])
+def test_dropout_is_unbiased_over_masks(p, causal, masks):
+    """Dropout leaves the output and the gradients unbiased: over the masks
+    the generator draws (distinct seeds), O, dQ, dK and dV average to those
+    of attention without dropout (O1 and dV1 are O and dV for V = 1 and
+    dO = 1: the row and column sums of the kept weights, the outputs with the
+    least sampling noise).  Each is projected on its undropped value,
+    s = <x, ref> / <ref, ref> per mask, and the mean of s must be 1 within six
+    standard errors (for p = 0.3 also element by element, which the rare
+    kept entries at p = 0.99 make too heavy-tailed for).  This fixes the
+    weight of the kept entries, 256 / t for a keep probability of t / 256 (t
+    the byte threshold), in the forward and in the backward: at p = 0.99,
+    t = 3 and 256 / t = 85.3, while the unquantised 1 / (1 - p) = 100 would
+    bias every output by 17% and no weight at all by a factor of 3 / 256;
+    both are shown to fall outside the bound on O1 (the forward's weight) and
+    dV1 (the backward's).  The finite-difference test above then ties dQ and
+    dK to the same weights."""
+    t = oracle.dropout_threshold(p)
+    samples, plain = _dropout_mask_average(p, 96, 8, masks, causal, seed_base=1000)
+    for name, x in samples.items():
+        ref = plain[name]
+        s = np.tensordot(x, ref, axes=ref.ndim) / np.sum(ref * ref)
+        mean, se = s.mean(), s.std(ddof=1) / np.sqrt(masks)
+        assert abs(mean - 1.0) < 6 * se, (name, mean, se)
+        if p > 0.9 and name in ("O1", "dV1"):
+            for wrong in (1.0 / (1.0 - p), 1.0):
+                ratio = wrong / (256.0 / t)
+                assert abs(mean * ratio - 1.0) > 6 * se * ratio, (name, wrong)
+        if p < 0.9:
+            z = np.abs(x.mean(axis=0) - ref) / np.maximum(x.std(axis=0, ddof=1) / np.sqrt(masks), 1e-12)
+            assert z.max() < 6.0, (name, float(z.max()))
+
+
 # --------------------------------------------------------------------------
 # Queries and keys of different lengths (shifted causal mask)
 # --------------------------------------------------------------------------

@@ -58,3 +58,34 @@ def test_sample_rows_covers_edges():
     s = sample_rows(1000, 20, seed=3)
     assert s[0] == 0 and s[-1] == 999 and 896 in s and 127 in s and 128 in s
     assert len(set(s.tolist())) == len(s)
+
+
+def test_report_figures_order():
+    """The per-element rule is the loosest and the tensor-RMS rule the
+    strictest reading of the max criterion; the enforced row rule lies
+    between them."""
+    from parity import errors
+    ref = _causal_like()
+    e = errors(_bf16(ref), ref)
+    assert e["max_elem"] <= e["max_row"] <= e["max_tensor"]
+    assert e["max_row"] <= TOL_MAX < e["max_tensor"]
+
+
+def test_collector_uses_one_rms_per_tensor():
+    """Pieces collected from several heads are judged against the RMS of all
+    of them: a head with tiny outputs cannot hide a large absolute error
+    behind its own small RMS, and a 1% scale error on one of two heads still
+    fails the mean criterion."""
+    import pytest
+    from parity import Parity
+    ref_a = _causal_like(seed=1)
+    ref_b = _causal_like(seed=2)
+    pc = Parity("ok")
+    pc.add("O", _bf16(ref_a), ref_a)
+    pc.add("O", _bf16(ref_b), ref_b)
+    pc.check()
+    pc = Parity("bad")
+    pc.add("O", ref_a * (1 + 1e-2), ref_a)
+    pc.add("O", ref_b, ref_b)
+    with pytest.raises(AssertionError):
+        pc.check()
