@@ -130,6 +130,168 @@ def whole_job_rate(world: int, units_per_rank: float, max_ms: float) -> float:
     return world * units_per_rank / (max_ms * 1e-3)
 
 
+def _timed_steps(stream, flush, fn, steps, warmup, nev):
+    """Run fn(None) `warmup` times, then `steps` times with an L2 flush before
+    each (outside the events) and nev CUDA events handed to fn; returns the
+    events.  The flush kernel itself runs once before the timed loop, so its
+    first launch is not inside the timed region."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn(None)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        fn(evs[i])
+    torch.cuda.synchronize()
+    return evs
+
+
+class _Problem:
+    """Device buffers of one dense workload and the calls of its steps."""
+
+    def __init__(self, w, dev, rank=0, Hkv=None):
+        import torch
+        import io_aware_exact_gb300 as attn
+        self.attn = attn
+        self.w = w
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.Hkv = Hkv or H
+        self.x = make_inputs(B, H, N, d, w.seed + 100 * rank, w.qk_mult, with_grad=True)
+        for n in ("k", "v"):          # grouped K / V heads: keep the first Hkv of each batch entry
+            self.x[n] = self.x[n][:, :self.Hkv].contiguous()
+        self.q, self.k, self.v, self.dO = (self.x[n].to(dev) for n in ("q", "k", "v", "dO"))
+        self.o = torch.empty_like(self.q)
+        self.o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.D = torch.empty_like(self.lse)
+        self.acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q), torch.empty_like(self.k),
+                                     torch.empty_like(self.v))
+        self.splits = (int(attn.lib().attn_gqa_split_hint(B, H, self.Hkv, N, int(w.causal)))
+                       if self.Hkv != H else 1)
+        self.part = (torch.empty((2, self.splits, B, self.Hkv, N, d), dtype=torch.float32,
+                                 device=dev) if self.splits > 1 else None)
+
+    def _args(self):
+        w = self.w
+        return w.B, w.H, w.N, w.d, w.causal, w.scale
+
+    def fwd(self, s):
+        P = lambda t: t.data_ptr()
+        B, H, N, d, causal, scale = self._args()
+        self.attn.attn_fwd(P(self.q), P(self.k), P(self.v), P(self.o), P(self.lse), B, H, N, d,
+                           causal, scale, s, Hkv=self.Hkv)
+
+    def bwd_main(self, s):
+        P = lambda t: t.data_ptr()
+        B, H, N, d, causal, scale = self._args()
+        if self.splits > 1:
+            self.attn._check(self.attn.lib().attn_bwd_gqa_split(
+                P(self.q), P(self.k), P(self.v), P(self.dO), P(self.lse), P(self.D), P(self.acc),
+                P(self.dq), P(self.dk), P(self.dv), P(self.part), self.splits, B, H, self.Hkv, N,
+                d, int(causal), scale, s), "attn_bwd_gqa_split")
+        else:
+            self.attn.attn_bwd(P(self.q), P(self.k), P(self.v), P(self.dO), P(self.lse), P(self.D),
+                               P(self.acc), P(self.dq), P(self.dk), P(self.dv), B, H, N, d, causal,
+                               scale, s, Hkv=self.Hkv)
+
+    def train_step(self, s, ev=None, stream=None):
+        """attn_fwd_train + attn_bwd_preprocess_o32 + attn_bwd; events between."""
+        P = lambda t: t.data_ptr()
+        B, H, N, d, causal, scale = self._args()
+        if ev:
+            ev[0].record(stream)
+        self.attn.attn_fwd_train(P(self.q), P(self.k), P(self.v), P(self.o), P(self.o32),
+                                 P(self.lse), B, H, N, d, causal, scale, s, Hkv=self.Hkv)
+        if ev:
+            ev[1].record(stream)
+        self.attn.attn_bwd_preprocess_o32(P(self.o32), P(self.dO), P(self.D), P(self.acc), B, H,
+                                          N, d, s)
+        if ev:
+            ev[2].record(stream)
+        self.bwd_main(s)
+        if ev:
+            ev[3].record(stream)
+
+    def exact_step(self, s, ev=None, stream=None):
+        """attn_fwd + attn_bwd_preprocess (D from recomputed P and dP) + attn_bwd."""
+        P = lambda t: t.data_ptr()
+        B, H, N, d, causal, scale = self._args()
+        if ev:
+            ev[0].record(stream)
+        self.fwd(s)
+        if ev:
+            ev[1].record(stream)
+        self.attn.attn_bwd_preprocess(P(self.q), P(self.k), P(self.v), P(self.dO), P(self.lse),
+                                      P(self.D), P(self.acc), B, H, N, d, causal, scale, s,
+                                      Hkv=self.Hkv)
+        if ev:
+            ev[2].record(stream)
+        self.bwd_main(s)
+        if ev:
+            ev[3].record(stream)
+
+
+def _mean(xs):
+    return sum(xs) / len(xs)
+
+
+def _workload_entry(w, dev, stream, flush, steps, warmup, peaks, with_cpu):
+    """Compact measurement of one more workload for the JSON line: the
+    training step (fwd+bwd workloads) or the forward (forward-only
+    workload, as latency), its roofline and a CPU sample of the oracle."""
+    import torch
+    prob = _Problem(w, dev)
+    s = int(stream.cuda_stream)
+    peak = peaks["bf16_tflops"]
+    fevs = _timed_steps(stream, flush, lambda ev: (ev and ev[0].record(stream), prob.fwd(s),
+                                                   ev and ev[1].record(stream)), steps, warmup, 2)
+    t_fwd = [e[0].elapsed_time(e[1]) for e in fevs]
+    ms_fwd = _mean(t_fwd)
+    entry = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+             "qk_mult": w.qk_mult, "seed": w.seed}
+    if not w.backward:
+        p = _percentiles(t_fwd)
+        entry.update({
+            "pass": "fwd", "latency_us_p10_p50_p90": [round(1000 * x, 2) for x in p],
+            "fwd_tflops": round(w.flops_fwd() / (p[1] * 1e-3) / 1e12, 3),
+            "roofline": {"kernel": "attn_fwd", "bound": "latency (%d CTAs for 152 SMs)" % (
+                w.B * w.H * ((w.N + 255) // 256)), "achieved": round(w.flops_fwd() / (p[1] * 1e-3) / 1e12, 3),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(w.flops_fwd() / (p[1] * 1e-3) / 1e12 / peak, 5)}})
+    else:
+        evs = _timed_steps(stream, flush, lambda ev: prob.train_step(s, ev, stream), steps, warmup, 4)
+        t_step = [e[0].elapsed_time(e[3]) for e in evs]
+        ms_step = _mean(t_step)
+        ms_bwd = _mean([e[2].elapsed_time(e[3]) for e in evs])
+        xevs = _timed_steps(stream, flush, lambda ev: prob.exact_step(s, ev, stream), steps, warmup, 4)
+        ms_exact = _mean([e[0].elapsed_time(e[3]) for e in xevs])
+        ms_exact_pre = _mean([e[1].elapsed_time(e[2]) for e in xevs])
+        fb = w.flops_fwd_bwd()
+        bwd_flops = 0.6 * fb
+        entry.update({
+            "pass": "fwd+bwd", "ms_per_step": round(ms_step, 4),
+            "tflops": round(fb / (ms_step * 1e-3) / 1e12, 2),
+            "frac_of_peak": round(fb / (ms_step * 1e-3) / 1e12 / peak, 4),
+            "fwd_ms": round(ms_fwd, 4), "fwd_tflops": round(w.flops_fwd() / (ms_fwd * 1e-3) / 1e12, 2),
+            "fwd_frac_of_peak": round(w.flops_fwd() / (ms_fwd * 1e-3) / 1e12 / peak, 4),
+            "fwd_train_ms": round(_mean([e[0].elapsed_time(e[1]) for e in evs]), 4),
+            "bwd_preprocess_o32_ms": round(_mean([e[1].elapsed_time(e[2]) for e in evs]), 4),
+            "step_exact_d_ms": round(ms_exact, 4), "bwd_preprocess_exact_d_ms": round(ms_exact_pre, 4),
+            "roofline": {"kernel": "attn_bwd (main kernel + dQ convert)", "bound": "tensor",
+                         "achieved": round(bwd_flops / (ms_bwd * 1e-3) / 1e12, 2), "peak": peak,
+                         "unit": "TFLOP/s",
+                         "frac": round(bwd_flops / (ms_bwd * 1e-3) / 1e12 / peak, 4)}})
+    if torch.cuda.is_available() and prob.attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during workload %s" % w.name)
+    if with_cpu:
+        entry["cpu_baseline"] = cpu_sample(w, prob.x)
+    del prob
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
     import io_aware_exact_gb300 as attn
@@ -144,51 +306,23 @@ def run_ours(args):
         pg = dist
     w = WORKLOADS[args.workload]
     B, H, N, d, causal = w.B, w.H, w.N, w.d, w.causal
-    x = make_inputs(B, H, N, d, w.seed + 100 * rank, w.qk_mult)
     Hkv = args.kv_heads or H
     if H % Hkv != 0:
         raise SystemExit("--kv-heads must divide the workload's %d heads" % H)
-    for n in ("k", "v"):          # grouped K / V heads: keep the first Hkv of each batch entry
-        x[n] = x[n][:, :Hkv].contiguous()
-    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
-    o = torch.empty_like(q)
-    o32 = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    D = torch.empty_like(lse)
-    acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    prob = _Problem(w, dev, rank, Hkv)
+    x = prob.x
+    q, k, v, dO = prob.q, prob.k, prob.v, prob.dO
+    o, lse, o32, D, acc = prob.o, prob.lse, prob.o32, prob.D, prob.acc
+    dq, dk, dv = prob.dq, prob.dk, prob.dv
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     s = int(stream.cuda_stream)
     scale = w.scale
-    P = lambda t: t.data_ptr()
-    # grouped heads: the group split over CTAs as the library suggests
-    splits = int(attn.lib().attn_gqa_split_hint(B, H, Hkv, N, int(causal))) if Hkv != H else 1
-    part = (torch.empty((2, splits, B, Hkv, N, d), dtype=torch.float32, device=dev)
-            if splits > 1 else None)
-
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        attn.attn_fwd_train(P(q), P(k), P(v), P(o), P(o32), P(lse), B, H, N, d, causal, scale, s,
-                            Hkv=Hkv)
-        if ev:
-            ev[1].record(stream)
-        attn.attn_bwd_preprocess_o32(P(o32), P(dO), P(D), P(acc), B, H, N, d, s)
-        if ev:
-            ev[2].record(stream)
-        if splits > 1:
-            attn._check(attn.lib().attn_bwd_gqa_split(
-                P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv), P(part), splits,
-                B, H, Hkv, N, d, int(causal), scale, s), "attn_bwd_gqa_split")
-        else:
-            attn.attn_bwd(P(q), P(k), P(v), P(dO), P(lse), P(D), P(acc), P(dq), P(dk), P(dv),
-                          B, H, N, d, causal, scale, s, Hkv=Hkv)
-        if ev:
-            ev[3].record(stream)
+    splits = prob.splits
 
     for _ in range(args.warmup):
-        step()
+        flush.zero_()   # the flush kernel's first launch also happens here, untimed
+        prob.train_step(s)
     torch.cuda.synchronize()
     if attn.attn_get_device_status() != 0:
         raise RuntimeError("device status set during warm-up")
@@ -201,7 +335,7 @@ def run_ours(args):
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()  # L2 flush between steps, outside the per-step events
-            step(evs[i])
+            prob.train_step(s, evs[i], stream)
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
@@ -216,19 +350,20 @@ def run_ours(args):
 
     # forward alone (attn_fwd: O and lse, no fp32 O), the inference forward,
     # timed per launch with the same L2 flush between launches
-    for _ in range(3):
-        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s, Hkv=Hkv)
-    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        fevs[i][0].record(stream)
-        attn.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, s, Hkv=Hkv)
-        fevs[i][1].record(stream)
-    torch.cuda.synchronize()
+    fevs = _timed_steps(stream, flush, lambda ev: (ev and ev[0].record(stream), prob.fwd(s),
+                                                   ev and ev[1].record(stream)),
+                        args.steps, 3, 2)
     if attn.attn_get_device_status() != 0:
         raise RuntimeError("device status set during the forward-only launches")
     ms_fwd_only = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in fevs), dev)
+
+    # the same step with D computed from recomputed P and dP (attn_fwd +
+    # attn_bwd_preprocess + attn_bwd, no fp32 O), for comparison
+    xevs = _timed_steps(stream, flush, lambda ev: prob.exact_step(s, ev, stream), args.steps, 3, 4)
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during the exact-D steps")
+    ms_exact = statistics.mean(e[0].elapsed_time(e[3]) for e in xevs)
+    ms_exact_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in xevs)
 
     # end to end through the public API: pinned host inputs in, results out.
     # Steps are pipelined over two buffer sets and three streams, as a user
@@ -303,10 +438,10 @@ def run_ours(args):
         for n, t in (("o", ro), ("lse", rl), ("dk", rk), ("dv", rv)):
             if not torch.equal(last[n], t.cpu()):
                 raise RuntimeError("end-to-end result %s differs from the device-resident step" % n)
-        del ro, rl, r32, rk, rv
+        del ro, rl, r32, rk, rv, bufs
         ms_e2e = ea.elapsed_time(eb) / args.e2e_steps
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
-        d2h = sum(t.numel() * t.element_size() for t in bufs[0]["host"].values())
+        d2h = sum(t.numel() * t.element_size() for n, t in res)
         e2e = {"value": round(world * w.flops_fwd_bwd() / (ms_e2e * 1e-3) / 1e12, 2),
                "unit": "TFLOPS", "ms_per_step": round(ms_e2e, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -323,6 +458,10 @@ def run_ours(args):
     # algorithmic work = 5 MMAs x 2 N^2 d per head, halved for causal
     flops_bwd_kernel = 10.0 * B * H * N * N * d / (2 if causal else 1)
     bwd_tflops = flops_bwd_kernel / (ms_bwd * 1e-3) / 1e12
+    # One denominator for every fraction: the burst bf16 peak.  The timed
+    # regions are tens of milliseconds at full SM clock, the regime the burst
+    # figure was measured in; the sustained figure (seconds under the power
+    # cap, at a lower clock) is given beside the step's fraction, labelled.
     peak_sus = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
     # the committed ncu summary is of the multi-head headline workload
@@ -347,20 +486,26 @@ def run_ours(args):
                    "causal": causal,
                    "global_batch": B * world, "seq_len": N,
                    "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs 268 MB > 126 MB L2, and L2 flushed (512 MB write) between steps",
+                   "l2": "inputs 268 MB > 126 MB L2, and L2 flushed (252 MB write) between steps",
                    "flop_convention": "fwd 4BHN^2d, fwd+bwd 10BHN^2d, halved for causal"},
-        "frac_of_peak": round(tflops_fb / peak_sus, 4),
+        "frac_of_peak": round(tflops_fb / peak_burst, 4),
+        "peak": peak_burst, "peak_kind": "bf16 burst, %s" % peaks["source"],
+        "frac_of_sustained_peak": round(tflops_fb / peak_sus, 4),
         "fwd": {"kernel": "attn_fwd (O, lse)", "tflops": round(tflops_fwd, 2),
                 "ms": round(ms_fwd_only, 4), "frac_of_peak": round(tflops_fwd / peak_burst, 4),
                 "peak": peak_burst, "peak_kind": "bf16 burst, %s" % peaks["source"]},
         "fwd_train": {"kernel": "attn_fwd_train (O, fp32 O, lse), inside the step",
                       "tflops": round(tflops_fwd_train, 2), "ms": round(ms_fwd, 4)},
-        "fwd_bwd_14x_tflops": round(world * 14.0 * B * H * N * N * d / 2 / (ms_step * 1e-3) / 1e12, 2),
+        "fwd_bwd_14x_tflops": round(world * 14.0 * B * H * N * N * d / (2 if causal else 1)
+                                    / (ms_step * 1e-3) / 1e12, 2),
         "bwd_preprocess_ms": round(statistics.mean(t_pre), 4),
+        "step_exact_d": {"path": "attn_fwd + attn_bwd_preprocess (D from recomputed P, dP) + attn_bwd",
+                         "ms": round(ms_exact, 4), "preprocess_ms": round(ms_exact_pre, 4),
+                         "tflops": round(flops_fb / (ms_exact * 1e-3) / 1e12, 2)},
         "roofline": {"kernel": "attn_bwd (main kernel + dQ convert)", "bound": "tensor",
-                     "achieved": round(bwd_tflops, 2), "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": round(bwd_tflops / peak_sus, 4), "traffic": traffic,
-                     "peak_kind": "bf16 sustained, %s" % peaks["source"]},
+                     "achieved": round(bwd_tflops, 2), "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": round(bwd_tflops / peak_burst, 4), "traffic": traffic,
+                     "peak_kind": "bf16 burst, %s" % peaks["source"]},
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
@@ -371,6 +516,16 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
+    # The other workloads, each timed the same way (fwd+bwd ones as the
+    # training step, the forward-only one as per-launch latency), one GPU only.
+    if world == 1 and not args.no_workloads and Hkv == H:
+        del prob, x, q, k, v, dO, o, lse, o32, D, acc, dq, dk, dv
+        torch.cuda.empty_cache()
+        line["workloads"] = [
+            _workload_entry(WORKLOADS[n], dev, stream, flush, max(args.steps, 20), args.warmup,
+                            peaks, not args.no_cpu_baseline)
+            for n in sorted(WORKLOADS, key=lambda n: (WORKLOADS[n].N, WORKLOADS[n].d))
+            if n != args.workload]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
@@ -459,6 +614,46 @@ def cpu_baseline(w, nheads):
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%d of %d heads (b=0), all rows, fwd+bwd, %.1f s" % (
                 len(heads), w.B * w.H, secs)}
+
+
+def cpu_sample(w, x=None):
+    """The oracle on a bounded sample of workload w, in the graded FLOP
+    convention: whole heads while they take under ~2 s (all rows, fwd and,
+    for training workloads, bwd), else 128 query rows and 128 key columns of
+    head (0, 0) with the most visible pairs."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    if x is None:
+        x = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_grad=True)
+    per_head = (w.flops_fwd_bwd() if w.backward else w.flops_fwd()) / (w.B * w.H)
+    if per_head < 2e10:
+        heads = [(0, h) for h in range(min(w.H, max(1, int(4e10 // per_head))))]
+        f = lambda t: t.float().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        for (b, h) in heads:
+            qh, kh, vh, dOh = (f(x[n][b, h]) for n in ("q", "k", "v", "dO"))
+            oracle.attention_forward(qh, kh, vh, w.causal, w.scale)
+            if w.backward:
+                oracle.attention_backward(qh, kh, vh, dOh, w.causal, w.scale)
+        secs = time.perf_counter() - t0
+        return {"value": round(per_head * len(heads) / secs / 1e12, 6), "unit": "TFLOPS",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": "%d of %d heads, all rows, %s, %.2f s" % (
+                    len(heads), w.B * w.H, "fwd+bwd" if w.backward else "fwd", secs)}
+    n = 128
+    rows = np.arange(w.N - n, w.N, dtype=np.int64)
+    cols = np.arange(0, n, dtype=np.int64)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    qh, kh, vh, dOh = (f(x[nm][0, 0]) for nm in ("q", "k", "v", "dO"))
+    lse_all, D_all, _ = oracle.attention_backward_rows(qh, kh, vh, dOh, w.causal, w.scale,
+                                                       with_dq=False)
+    secs = _ref_sample(w, x, rows, cols, lse_all, D_all)
+    pairs = (float(np.sum(rows + 1)) + float(np.sum(w.N - cols))) if w.causal else 2.0 * n * w.N
+    return {"value": round(10.0 * w.d * pairs / 2.0 / secs / 1e12, 6), "unit": "TFLOPS",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "head (0,0): last %d query rows and first %d key columns, fwd+bwd, %.2f s" % (
+                n, n, secs)}
 
 
 def _ref_sample(w, x, rows, cols, lse_all, D_all):
@@ -838,6 +1033,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the named workload (by default the JSON line also carries "
+                         "every other workload's numbers under \"workloads\")")
     ap.add_argument("--varlen", action="store_true",
                     help="time the step on a packed variable-length batch instead")
     ap.add_argument("--dropout", type=float, default=0.0,

@@ -38,6 +38,11 @@
  *    ATTN_ERR_TIMEOUT in the library's device status word, read with
  *    attn_get_device_status().
  *  - Return value: an attn_status code (0 = success).  Nothing throws.
+ *  - Per device, the first call looks up the device addresses of the
+ *    library's status word (and, for attn_bwd_noalloc, of its workspace
+ *    array) and keeps them for the life of the process.  Resetting a device
+ *    (cudaDeviceReset) invalidates those addresses: do not call the library
+ *    on a device after resetting it in the same process.
  */
 #ifndef IO_AWARE_EXACT_GB300_ATTN_H
 #define IO_AWARE_EXACT_GB300_ATTN_H
@@ -161,6 +166,9 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO,
  *  - The first call on a device looks the array's device address up (once
  *    per device, with that device current); make that first call before
  *    capturing a stream into a graph.
+ *  - The looked-up address is kept for the life of the process, so calling
+ *    this entry point on a device after a cudaDeviceReset of that device is
+ *    not supported (see the shared conventions above).
  *  - All calls on a device share the one array.  Each call overwrites D and
  *    zeroes the accumulator before use, so earlier contents do not matter,
  *    but calls whose kernels overlap on the GPU (different streams without

@@ -203,16 +203,8 @@ __device__ __forceinline__ int grid_block() {
     return static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
 }
 
-inline int device_sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 152;
-    }
-    return n;
-}
+// SM count of the current device (cached per device index; thread-safe).
+int device_sm_count();
 
 // K / V head of (batch, query head) bh when groups of H / Hkv query heads share one
 __device__ __forceinline__ int kv_head(int bh, int H, int Hkv) {
