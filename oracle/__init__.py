@@ -271,6 +271,60 @@ def attention_backward_varlen(q, k, v, dO, cu_seqlens, causal: bool, scale: floa
     return dq, dk, dv
 
 
+def attention_forward_varlen_qk(q, k, v, cu_q, cu_k, max_seqlen_q: int, causal: bool,
+                                scale: float):
+    """Packed batch whose keys have lengths of their own: q [total_q, H, d]
+    with sequence b at rows [cu_q[b], cu_q[b+1]), k, v [total_k, Hkv, *] with
+    its keys at rows [cu_k[b], cu_k[b+1]).  Each sequence attends only to its
+    own keys; with ``causal`` the mask is aligned bottom-right (key j visible
+    to query i iff j <= i + Lk - Lq, attention_forward_offset).  Returns O
+    [total_q, H, dv] and lse [B, H, max_seqlen_q] (NaN past each length)."""
+    cq, ck = _seq_bounds(cu_q), _seq_bounds(cu_k)
+    assert len(cq) == len(ck)
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, H, _ = q.shape
+    Hkv = k.shape[1]
+    B = len(cq) - 1
+    o = np.zeros((total, H, v.shape[2]), np.float64)
+    lse = np.full((B, H, max_seqlen_q), np.nan, np.float64)
+    for b in range(B):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            ob, lb = attention_forward_offset(q[q0:q1, h], k[k0:k1, g], v[k0:k1, g], causal, scale,
+                                              (k1 - k0) - (q1 - q0))
+            o[q0:q1, h] = ob
+            lse[b, h, :q1 - q0] = lb
+    return o, lse
+
+
+def attention_backward_varlen_qk(q, k, v, dO, cu_q, cu_k, causal: bool, scale: float):
+    """(dQ [total_q, H, d], dK [total_k, Hkv, d], dV [total_k, Hkv, dv]) of
+    attention_forward_varlen_qk: per sequence and head the single-head
+    backward with the shifted causal mask; dK, dV sum over each group."""
+    cq, ck = _seq_bounds(cu_q), _seq_bounds(cu_k)
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    H, Hkv = q.shape[1], k.shape[1]
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(k.shape, np.float64)
+    dv = np.zeros(v.shape, np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        for h in range(H):
+            g = kv_head_of(h, H, Hkv)
+            dqb, dkb, dvb, _, _ = attention_backward_offset(q[q0:q1, h], k[k0:k1, g], v[k0:k1, g],
+                                                            dO[q0:q1, h], causal, scale,
+                                                            (k1 - k0) - (q1 - q0))
+            dq[q0:q1, h] = dqb
+            dk[k0:k1, g] += dkb
+            dv[k0:k1, g] += dvb
+    return dq, dk, dv
+
+
 def expand_block_mask(block_mask, nq: int, nk: int, block: int, causal: bool) -> np.ndarray:
     """Element visibility [nq, nk] (True = key j enters row i's softmax) of a
     block-sparse layout: block_mask [ceil(nq / block), ceil(nk / block)], a
@@ -301,7 +355,7 @@ def attention_forward_masked(q, k, v, visible, scale: float):
     s = scale * (q @ k.T)
     s = np.where(vis, s, -np.inf)
     has = vis.any(axis=1)
-    m = np.where(has, s.max(axis=1), 0.0)
+    m = np.where(has, s.max(axis=1, initial=-np.inf), 0.0)     # (no keys at all: every row empty)
     e = np.where(vis, np.exp(s - m[:, None]), 0.0)
     z = e.sum(axis=1)
     p = np.where(has[:, None], e / np.where(has, z, 1.0)[:, None], 0.0)
@@ -319,7 +373,7 @@ def attention_backward_masked(q, k, v, dO, visible, scale: float):
     vis = np.asarray(visible, dtype=bool)
     s = np.where(vis, scale * (q @ k.T), -np.inf)
     has = vis.any(axis=1)
-    m = np.where(has, s.max(axis=1), 0.0)
+    m = np.where(has, s.max(axis=1, initial=-np.inf), 0.0)
     e = np.where(vis, np.exp(s - m[:, None]), 0.0)
     z = np.where(has, e.sum(axis=1), 1.0)
     p = e / z[:, None]

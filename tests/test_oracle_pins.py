@@ -397,6 +397,80 @@ def test_varlen_backward_matches_finite_differences():
         assert np.max(np.abs(got - want)) / scale < 1e-6
 
 
+def _packed_qk_attention(q, k, v, cu_q, cu_k, causal, tau):
+    """Brute force over the whole packed batch: one softmax per packed query
+    row over every packed key row, with a mask that allows only the row's own
+    sequence and, when causal, keys at position <= query position + Lk - Lq."""
+    nq, nk = len(q), len(k)
+    sq = np.searchsorted(cu_q, np.arange(nq), side="right") - 1
+    sk = np.searchsorted(cu_k, np.arange(nk), side="right") - 1
+    pq = np.arange(nq) - np.asarray(cu_q)[sq]
+    pk = np.arange(nk) - np.asarray(cu_k)[sk]
+    lq = np.diff(cu_q)[sq]
+    lk = np.diff(cu_k)[sk]
+    H, Hkv = q.shape[1], k.shape[1]
+    o = np.zeros((nq, H, v.shape[2]))
+    for h in range(H):
+        g = h // (H // Hkv)
+        allowed = sq[:, None] == sk[None, :]
+        if causal:
+            allowed &= pk[None, :] <= pq[:, None] + lk[None, :] - lq[:, None]
+        s = np.where(allowed, tau * q[:, h] @ k[:, g].T, -np.inf)
+        has = allowed.any(axis=1)
+        m = np.where(has, s.max(axis=1), 0.0)
+        p = np.where(allowed, np.exp(s - m[:, None]), 0.0)
+        z = np.where(has, p.sum(axis=1), 1.0)
+        o[:, h] = (p / z[:, None]) @ v[:, g]
+    return o
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_qk_forward_matches_packed_mask(causal):
+    """Keys of their own lengths: 5 queries against 8 keys (a query chunk
+    after 3 earlier keys), 6 against 2 (the first 4 queries see no key under
+    the bottom-right mask: O = 0, lse = -inf), an empty query set with 3 keys,
+    1 against 1, and 2 queries without keys; every row equals brute-force
+    attention over the whole packed batch with the sequence and shifted
+    causal mask written out."""
+    r = _rng(75 + int(causal))
+    cu_q, cu_k = [0, 5, 11, 11, 12, 14], [0, 8, 10, 13, 14, 14]
+    q, k, v = r.normal(size=(14, 4, 3)), r.normal(size=(14, 2, 3)), r.normal(size=(14, 2, 2))
+    o, lse = oracle.attention_forward_varlen_qk(q, k, v, cu_q, cu_k, 6, causal, 0.7)
+    want = _packed_qk_attention(q, k, v, np.array(cu_q), np.array(cu_k), causal, 0.7)
+    assert np.max(np.abs(o - want)) < 1e-12
+    if causal:
+        assert np.all(o[5:9] == 0.0) and np.all(lse[1, :, :4] == -np.inf)
+        assert np.all(np.isfinite(lse[1, :, 4:6]))
+    assert np.all(np.isnan(lse[2]))
+    # the last sequence has 2 queries and no keys: empty rows, causal or not
+    assert np.all(o[12:14] == 0.0) and np.all(lse[4, :, :2] == -np.inf)
+    # equal lengths: the packed function of one cu_seqlens
+    cu = [0, 3, 7]
+    q2, k2, v2 = r.normal(size=(7, 2, 3)), r.normal(size=(7, 1, 3)), r.normal(size=(7, 1, 2))
+    a, la = oracle.attention_forward_varlen_qk(q2, k2, v2, cu, cu, 4, causal, 0.7)
+    b, lb = oracle.attention_forward_varlen(q2, k2, v2, cu, 4, causal, 0.7)
+    assert np.max(np.abs(a - b)) < 1e-13 and np.allclose(la, lb, equal_nan=True)
+
+
+def test_varlen_qk_backward_matches_finite_differences():
+    r = _rng(80)
+    cu_q, cu_k = [0, 3, 7], [0, 5, 7]      # 3 queries on 5 keys; 4 queries on 2 keys
+    q, dO = r.normal(size=(7, 2, 3)), r.normal(size=(7, 2, 2))
+    k, v = r.normal(size=(7, 1, 3)), r.normal(size=(7, 1, 2))
+
+    def loss(qq, kk, vv):
+        return float(np.sum(_packed_qk_attention(qq, kk, vv, np.array(cu_q), np.array(cu_k),
+                                                 True, 0.7) * dO))
+
+    dq, dk, dv = oracle.attention_backward_varlen_qk(q, k, v, dO, cu_q, cu_k, True, 0.7)
+    assert np.all(dq[3:5] == 0.0)          # rows that see no key
+    for got, want in ((dq, _fd_grad(q, lambda x: loss(x, k, v))),
+                      (dk, _fd_grad(k, lambda x: loss(q, x, v))),
+                      (dv, _fd_grad(v, lambda x: loss(q, k, x)))):
+        scale = max(1.0, np.max(np.abs(want)))
+        assert np.max(np.abs(got - want)) / scale < 1e-6
+
+
 # --------------------------------------------------------------------------
 # Block-sparse layouts (numpy fp64 functions of the oracle)
 # --------------------------------------------------------------------------
