@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import check_lse, check_tensor
+from parity import check_lse, check_tensor, dtype_name
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +68,8 @@ def _compare(x, mask, out, causal, scale):
     check_lse(lse[~empty], ref["lse"][~empty])
     assert np.all(out["o_plain"].float().numpy()[empty] == 0.0)
     for n in ("o", "o_plain", "dq", "dk", "dv"):
-        check_tensor(n, _f64(out[n]).reshape(-1, d), ref[n[:1] if n == "o_plain" else n].reshape(-1, d))
+        check_tensor(n, _f64(out[n]).reshape(-1, d), ref[n[:1] if n == "o_plain" else n].reshape(-1, d),
+                     dtype=dtype_name(x["q"]))
     return ref, empty
 
 

@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import Parity, check_tensor
+from parity import Parity, check_tensor, dtype_name
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def _run(x, causal, scale, path, splits=None):
 
 def _compare(x, out, causal, scale):
     B = x["q"].shape[0]
-    pc = Parity("grouped")
+    pc = Parity("grouped", dtype_name(x["q"]))
     for b in range(B):
         q, k, v, dO = (_f64(x[n][b]) for n in ("q", "k", "v", "dO"))
         o_ref, lse_ref = oracle.attention_forward_grouped(q, k, v, causal, scale)

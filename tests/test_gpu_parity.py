@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300.inputs import WORKLOADS, make_inputs
-from parity import Parity, check_tensor, sample_rows
+from parity import Parity, check_tensor, dtype_name, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -75,7 +75,7 @@ def _compare_head(x, out, b, h, causal, scale, backward, pc, rows=None, cols=Non
 
 def _compare_heads(x, out, heads, causal, scale, backward, label, rows=None, cols=None):
     """Compare the listed heads; each tensor is judged over all of them at once."""
-    pc = Parity(label)
+    pc = Parity(label, dtype_name(x["q"]))
     for (b, h) in heads:
         _compare_head(x, out, b, h, causal, scale, backward, pc, rows=rows, cols=cols)
     pc.check()

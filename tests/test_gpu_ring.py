@@ -17,7 +17,7 @@ import oracle
 import io_aware_exact_gb300 as attn
 from io_aware_exact_gb300 import ring
 from io_aware_exact_gb300.inputs import make_inputs
-from parity import Parity, check_lse, check_tensor
+from parity import Parity, check_lse, check_tensor, dtype_name
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def test_ring_equals_whole_sequence(R, N, d, causal, dtype):
     assert attn.attn_get_device_status() == 0
     got = {n: torch.cat(t, dim=2) for n, t in
            (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    pc = Parity("ring R=%d" % R)
+    pc = Parity("ring R=%d" % R, dtype_name(dtype))
     for h in range(H):
         q, k, v, dO = (_f64(x[n][0, h]) for n in ("q", "k", "v", "dO"))
         o_ref, lse_ref = oracle.attention_forward(q, k, v, causal, scale)

@@ -15,7 +15,7 @@ torch = pytest.importorskip("torch")
 
 import oracle
 import io_aware_exact_gb300 as attn
-from parity import Parity, check_tensor
+from parity import Parity, check_tensor, dtype_name
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def _compare(x, cu, max_s, out, causal, scale):
     o_ref, lse_ref = oracle.attention_forward_varlen(q, k, v, cu, max_s, causal, scale)
     dq_ref, dk_ref, dv_ref = oracle.attention_backward_varlen(q, k, v, dO, cu, causal, scale)
     lse = out["lse"].numpy().astype(np.float64)
-    pc = Parity("varlen")
+    pc = Parity("varlen", dtype_name(x["q"]))
     for b in range(len(cu) - 1):
         s0, s1 = int(cu[b]), int(cu[b + 1])
         assert np.all(lse[b, :, s1 - s0:] == SENTINEL), "lse past the sequence was written"
