@@ -269,7 +269,9 @@ def _workload_entry(w, dev, stream, flush, steps, warmup, peaks, with_cpu):
         ms_exact = _mean([e[0].elapsed_time(e[3]) for e in xevs])
         ms_exact_pre = _mean([e[1].elapsed_time(e[2]) for e in xevs])
         fb = w.flops_fwd_bwd()
-        bwd_flops = 0.6 * fb
+        # the backward kernel's algorithmic work: 5 MMAs x 2 N^2 d per head
+        # (S and dP recomputed, dV, dK, dQ), halved for causal
+        bwd_flops = 10.0 * w.B * w.H * w.N * w.N * w.d / (2 if w.causal else 1)
         entry.update({
             "pass": "fwd+bwd", "ms_per_step": round(ms_step, 4),
             "tflops": round(fb / (ms_step * 1e-3) / 1e12, 2),

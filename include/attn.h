@@ -293,6 +293,57 @@ int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void*
                         float scale, void* stream);
 
 /*
+ * Packed batches whose keys have lengths of their own (Lk != Lq per
+ * sequence: a query chunk that attends to a longer key prefix, or queries
+ * against a shorter set of keys).  The sj-techlog page's packed interface
+ * (section "2. module 경계는 ...") passes one cu_seqlens and one max_s for q,
+ * k and v together; the paldyn.com survey's version table ("v1에서 v3까지")
+ * lists variable-length inputs among FlashAttention-2's additions.  Reading
+ * taken here: queries and keys each get their own offsets and maximum.
+ *  - q, o, dO, dq, o32, dq_accum: [total_q, H, d]; k, v, dk, dv:
+ *    [total_k, Hkv, d].  Sequence b's queries are rows [cu_seqlens_q[b],
+ *    cu_seqlens_q[b+1]) and its keys rows [cu_seqlens_k[b],
+ *    cu_seqlens_k[b+1]) (both device int32 [B + 1], as cu_seqlens above).
+ *  - Causal mask aligned bottom-right: with Lq queries and Lk keys, key j is
+ *    visible to query i iff j <= i + Lk - Lq, so the last query sees every
+ *    key.  With Lq = Lk this is the top-left mask of the other entry points.
+ *    A query that sees no key (i < Lq - Lk) gets O = 0, lse = -inf and
+ *    dQ = 0; keys of a sequence without queries get dK = dV = 0.
+ *  - lse: [B, H, max_seqlen_q]; D: [total_q, H] (attn_bwd_preprocess_o32_varlen
+ *    with total = total_q serves both paths).
+ *  - max_seqlen_q / max_seqlen_k must be >= every query / key length.
+ * Argument errors as for attn_fwd_varlen, plus a NULL or misaligned
+ * cu_seqlens_k, total_k < 0 or max_seqlen_k outside 1..2^24.
+ */
+int attn_fwd_varlen_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                       const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int total_q,
+                       int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
+                       int causal, float scale, void* stream);
+int attn_fwd_varlen_qk_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int total_q,
+                           int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
+                           int causal, float scale, void* stream);
+int attn_fwd_train_varlen_qk(const void* q, const void* k, const void* v, void* o, float* o32,
+                             float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                             int Hkv, int d, int causal, float scale, void* stream);
+int attn_fwd_train_varlen_qk_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                                 float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                 int B, int total_q, int total_k, int max_seqlen_q,
+                                 int max_seqlen_k, int H, int Hkv, int d, int causal, float scale,
+                                 void* stream);
+int attn_bwd_varlen_qk(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                       void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                       int Hkv, int d, int causal, float scale, void* stream);
+int attn_bwd_varlen_qk_f16(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                           void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                           int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                           int Hkv, int d, int causal, float scale, void* stream);
+
+/*
  * Block-sparse layouts.  The sj-techlog page (section "대안, 비교와 선택
  * 기준") describes block-sparse FlashAttention: a block mask fixed in advance,
  * whose zero blocks are skipped.  Here the block is one 128 x 128 tile:

@@ -87,6 +87,18 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = at
                 fn.restype = I
+            # keys of their own lengths: (cu_seqlens_q, cu_seqlens_k, B, total_q, total_k,
+            # max_seqlen_q, max_seqlen_k, H, Hkv, d, causal, scale, stream)
+            kvt = [P, P, I, I, I, I, I, I, I, I, I, F, P]
+            for name, at in (("attn_fwd_varlen_qk", [P] * 5 + kvt),
+                             ("attn_fwd_varlen_qk_f16", [P] * 5 + kvt),
+                             ("attn_fwd_train_varlen_qk", [P] * 6 + kvt),
+                             ("attn_fwd_train_varlen_qk_f16", [P] * 6 + kvt),
+                             ("attn_bwd_varlen_qk", [P] * 10 + kvt),
+                             ("attn_bwd_varlen_qk_f16", [P] * 10 + kvt)):
+                fn = getattr(L, name)
+                fn.argtypes = at
+                fn.restype = I
             # block-sparse layouts: (block_mask, mask_head_stride) before B
             LL = ctypes.c_longlong
             sfwd = [P, P, P, P, P, P, LL, I, I, I, I, I, F, P]
@@ -523,7 +535,15 @@ AttnFunction = None
 # Packed variable-length batches
 # ---------------------------------------------------------------------------
 
-def _check_varlen(q, k, v, cu_seqlens, *qlike):
+def _check_cu(cu, B=None):
+    torch = _torch()
+    if cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_cuda or cu.numel() < 2:
+        raise ValueError("cu_seqlens must be a CUDA int32 vector of B + 1 offsets")
+    if B is not None and cu.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
+
+
+def _check_varlen(q, k, v, cu_seqlens, *qlike, own_keys=False):
     torch = _torch()
     for t in (q, k, v) + qlike:
         if t.dim() != 3 or not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
@@ -531,51 +551,68 @@ def _check_varlen(q, k, v, cu_seqlens, *qlike):
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise ValueError("expected bfloat16 or float16 tensors")
     total, H, d = q.shape
-    if k.shape != v.shape or k.shape[0] != total or k.shape[2] != d:
-        raise ValueError("k, v must be [total, Hkv, d] like q")
+    if k.shape != v.shape or k.shape[2] != d or (not own_keys and k.shape[0] != total):
+        raise ValueError("k, v must be [total, Hkv, d] like q (total_k rows with cu_seqlens_k)")
     for t in qlike:
         if t.shape != q.shape:
             raise ValueError("dO must be shaped like q")
-    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda
-            or cu_seqlens.numel() < 2):
-        raise ValueError("cu_seqlens must be a CUDA int32 vector of B + 1 offsets")
+    _check_cu(cu_seqlens)
     return (cu_seqlens.numel() - 1, total, H, k.shape[1], d), q.dtype == torch.float16
 
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale=None,
-                   o=None, lse=None, o32=None, stream=None):
+                   o=None, lse=None, o32=None, stream=None, cu_seqlens_k=None, max_seqlen_k=None):
     """O [total, H, d] and lse [B, H, max_seqlen] of a packed variable-length
     batch (sequence b is tokens cu_seqlens[b]:cu_seqlens[b+1] of q, k, v).
     With ``o32`` (True or an fp32 [total, H, d] tensor) the training forward
-    also writes O in fp32 and returns (o, lse, o32)."""
+    also writes O in fp32 and returns (o, lse, o32).  With ``cu_seqlens_k``
+    (and ``max_seqlen_k``) the keys have lengths of their own: k, v are
+    [total_k, Hkv, d], sequence b's keys are rows cu_seqlens_k[b]:
+    cu_seqlens_k[b+1], and the causal mask is aligned bottom-right."""
     torch = _torch()
-    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens)
+    own = cu_seqlens_k is not None
+    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens, own_keys=own)
     scale = d ** -0.5 if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     if lse is None:
         lse = torch.empty((B, H, max_seqlen), dtype=torch.float32, device=q.device)
     s = _stream_handle(stream)
-    args = (cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d, int(bool(causal)), scale, s)
+    if own:
+        _check_cu(cu_seqlens_k, B)
+        if max_seqlen_k is None:
+            raise ValueError("max_seqlen_k is needed with cu_seqlens_k")
+        args = (cu_seqlens.data_ptr(), cu_seqlens_k.data_ptr(), B, total, k.shape[0],
+                int(max_seqlen), int(max_seqlen_k), H, Hkv, d, int(bool(causal)), scale, s)
+        suffix = "_qk"
+    else:
+        args = (cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d, int(bool(causal)),
+                scale, s)
+        suffix = ""
     L = lib()
     if o32 is None:
-        fn = L.attn_fwd_varlen_f16 if f16 else L.attn_fwd_varlen
+        name = "attn_fwd_varlen" + suffix
+        fn = getattr(L, name + ("_f16" if f16 else ""))
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), *args),
-               "attn_fwd_varlen")
+               name)
         return o, lse
     if o32 is True:
         o32 = torch.empty((total, H, d), dtype=torch.float32, device=q.device)
-    fn = L.attn_fwd_train_varlen_f16 if f16 else L.attn_fwd_train_varlen
+    name = "attn_fwd_train_varlen" + suffix
+    fn = getattr(L, name + ("_f16" if f16 else ""))
     _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o32.data_ptr(),
-              lse.data_ptr(), *args), "attn_fwd_train_varlen")
+              lse.data_ptr(), *args), name)
     return o, lse, o32
 
 
 def backward_varlen(q, k, v, o32, lse, dO, cu_seqlens, max_seqlen: int, causal: bool = False,
-                    scale=None, dq=None, dk=None, dv=None, D=None, dq_accum=None, stream=None):
+                    scale=None, dq=None, dk=None, dv=None, D=None, dq_accum=None, stream=None,
+                    cu_seqlens_k=None, max_seqlen_k=None):
     """dQ, dK, dV of a packed variable-length batch, from the training
-    forward's fp32 O and lse (D = rowsum(dO o O))."""
+    forward's fp32 O and lse (D = rowsum(dO o O)); ``cu_seqlens_k`` and
+    ``max_seqlen_k`` as for forward_varlen."""
     torch = _torch()
-    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens, dO)
+    own = cu_seqlens_k is not None
+    (B, total, H, Hkv, d), f16 = _check_varlen(q, k, v, cu_seqlens, dO, own_keys=own)
     scale = d ** -0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -588,9 +625,18 @@ def backward_varlen(q, k, v, o32, lse, dO, cu_seqlens, max_seqlen: int, causal: 
     pre = L.attn_bwd_preprocess_o32_varlen_f16 if f16 else L.attn_bwd_preprocess_o32_varlen
     _check(pre(o32.data_ptr(), dO.data_ptr(), D.data_ptr(), dq_accum.data_ptr(), total, H, d, s),
            "attn_bwd_preprocess_o32_varlen")
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+            D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    if own:
+        _check_cu(cu_seqlens_k, B)
+        if max_seqlen_k is None:
+            raise ValueError("max_seqlen_k is needed with cu_seqlens_k")
+        fn = L.attn_bwd_varlen_qk_f16 if f16 else L.attn_bwd_varlen_qk
+        _check(fn(*ptrs, cu_seqlens.data_ptr(), cu_seqlens_k.data_ptr(), B, total, k.shape[0],
+                  int(max_seqlen), int(max_seqlen_k), H, Hkv, d, int(bool(causal)), scale, s),
+               "attn_bwd_varlen_qk")
+        return dq, dk, dv
     fn = L.attn_bwd_varlen_f16 if f16 else L.attn_bwd_varlen
-    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
-              D.data_ptr(), dq_accum.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-              cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d, int(bool(causal)),
-              scale, s), "attn_bwd_varlen")
+    _check(fn(*ptrs, cu_seqlens.data_ptr(), B, total, int(max_seqlen), H, Hkv, d,
+              int(bool(causal)), scale, s), "attn_bwd_varlen")
     return dq, dk, dv

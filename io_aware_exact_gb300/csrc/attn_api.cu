@@ -494,23 +494,49 @@ int check_varlen(const int* cu_seqlens, int B, int total, int max_seqlen, int H,
     return check_kv_heads(H, Hkv);
 }
 
+// Keys of their own lengths (cu_seqlens_k != nullptr): sequence b's keys are
+// rows [cu_seqlens_k[b], cu_seqlens_k[b+1]) of the [total_k, Hkv, d] K and V.
+struct VarlenKeys {
+    const int* cu_seqlens_k = nullptr;
+    int total_k = 0;
+    int max_seqlen_k = 0;
+};
+
+int check_varlen_keys(const VarlenKeys& kv, int Hkv) {
+    if (kv.cu_seqlens_k == nullptr) return ATTN_OK;
+    if (reinterpret_cast<uintptr_t>(kv.cu_seqlens_k) & 3u) return ATTN_ERR_INVALID_ARG;
+    if (kv.total_k < 0 || kv.max_seqlen_k < 1 || kv.max_seqlen_k > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(kv.total_k) * Hkv > 2147483647LL) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
 int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float* o32, float* lse,
                     const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d,
-                    int causal, float scale, void* stream, bool bf16) {
+                    int causal, float scale, void* stream, bool bf16, VarlenKeys kv = {}) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     int rc = check_varlen(cu_seqlens, B, total, max_seqlen, H, Hkv, d);
     if (rc) return rc;
+    if ((rc = check_varlen_keys(kv, Hkv))) return rc;
+    const bool own_keys = kv.cu_seqlens_k != nullptr;
+    const int total_k = own_keys ? kv.total_k : total;
     if ((rc = check_scale(scale))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         (o32 != nullptr && !aligned16(o32)))
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    if (total == 0) return ATTN_OK;   // no tokens: nothing to compute
+    if (total == 0) return ATTN_OK;   // no query tokens: nothing to compute
     CUtensorMap tq, tk, tv, to, to32;
-    if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&tk, k, total, Hkv, d, bf16)) ||
-        (rc = make_map_packed(&tv, v, total, Hkv, d, bf16)) || (rc = make_map_packed(&to, o, total, H, d, bf16)))
+    if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&to, o, total, H, d, bf16)))
         return rc;
+    if (total_k > 0) {
+        if ((rc = make_map_packed(&tk, k, total_k, Hkv, d, bf16)) ||
+            (rc = make_map_packed(&tv, v, total_k, Hkv, d, bf16)))
+            return rc;
+    } else {
+        tk = tq;   // no key rows at all: every CTA writes empty rows and loads nothing
+        tv = tq;
+    }
     if (o32 != nullptr) {
         if ((rc = make_map_packed_f32(&to32, o32, total, H, d))) return rc;
     } else {
@@ -529,6 +555,9 @@ int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float*
     a.cu_seqlens = cu_seqlens;
     a.total = total;
     a.max_seqlen = max_seqlen;
+    a.cu_seqlens_k = kv.cu_seqlens_k;
+    a.total_k = total_k;
+    a.max_seqlen_k = own_keys ? kv.max_seqlen_k : max_seqlen;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     return map_launch(launch_fwd(tq, tk, tv, to, to32, a, B * H, d, causal != 0, bf16,
@@ -560,11 +589,15 @@ int pre_o32_varlen_impl(const float* o32, const void* dO, float* D, float* dq_ac
 int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                     const float* D, float* dq_accum, void* dq, void* dk, void* dv,
                     const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv, int d,
-                    int causal, float scale, void* stream, bool bf16) {
+                    int causal, float scale, void* stream, bool bf16, VarlenKeys kv = {}) {
     if (!q || !k || !v || !dO || !lse || !D || !dq_accum || !dq || !dk || !dv)
         return ATTN_ERR_INVALID_ARG;
     int rc = check_varlen(cu_seqlens, B, total, max_seqlen, H, Hkv, d);
     if (rc) return rc;
+    if ((rc = check_varlen_keys(kv, Hkv))) return rc;
+    const bool own_keys = kv.cu_seqlens_k != nullptr;
+    const int total_k = own_keys ? kv.total_k : total;
+    const int max_seqlen_k = own_keys ? kv.max_seqlen_k : max_seqlen;
     if ((rc = check_scale(scale))) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
         !aligned16(D) || !aligned16(dq_accum) || !aligned16(dq) || !aligned16(dk) ||
@@ -572,14 +605,28 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* dO,
         return ATTN_ERR_MISALIGNED;
     int* status = nullptr;
     if ((rc = current_device(&status))) return rc;
-    if (total == 0) return ATTN_OK;
-    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
-    if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&tk, k, total, Hkv, d, bf16)) ||
-        (rc = make_map_packed(&tv, v, total, Hkv, d, bf16)) || (rc = make_map_packed(&tdo, dO, total, H, d, bf16)) ||
-        (rc = make_map_packed_f32(&tdq, dq_accum, total, H, d)) ||
-        (rc = make_map_packed(&tdk, dk, total, Hkv, d, bf16)) || (rc = make_map_packed(&tdv, dv, total, Hkv, d, bf16)))
-        return rc;
+    if (total == 0 && total_k == 0) return ATTN_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DqConvertArgs c{};
+    c.dq_accum = dq_accum;
+    c.dq = dq;
+    c.elems = static_cast<long long>(total) * H * d;
+    c.scale = scale;
+    // no key rows: dK, dV are empty and every dQ row is 0 (dq_accum was zeroed)
+    if (total_k == 0) return map_launch(launch_dq_convert(c, bf16, st));
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+    if ((rc = make_map_packed(&tk, k, total_k, Hkv, d, bf16)) || (rc = make_map_packed(&tv, v, total_k, Hkv, d, bf16)) ||
+        (rc = make_map_packed(&tdk, dk, total_k, Hkv, d, bf16)) || (rc = make_map_packed(&tdv, dv, total_k, Hkv, d, bf16)))
+        return rc;
+    if (total > 0) {
+        if ((rc = make_map_packed(&tq, q, total, H, d, bf16)) || (rc = make_map_packed(&tdo, dO, total, H, d, bf16)) ||
+            (rc = make_map_packed_f32(&tdq, dq_accum, total, H, d)))
+            return rc;
+    } else {
+        tq = tk;   // no query rows: every CTA writes dK = dV = 0 and loads no query
+        tdo = tk;
+        tdq = tk;
+    }
     BwdArgs a{};
     a.lse = lse;
     a.D = D;
@@ -592,21 +639,20 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* dO,
     a.H = H;
     a.Hkv = Hkv;
     a.BHkv = B * Hkv;
-    a.num_kvblocks = (max_seqlen + kTile - 1) / kTile;
+    a.num_kvblocks = (max_seqlen_k + kTile - 1) / kTile;
     a.cu_seqlens = cu_seqlens;
     a.total = total;
     a.max_seqlen = max_seqlen;
+    a.cu_seqlens_k = kv.cu_seqlens_k;
+    a.total_k = total_k;
+    a.max_seqlen_k = max_seqlen_k;
     a.scale = scale;
     a.scale_log2 = scale * kLog2e;
     a.wait_polls = kDefaultWaitPolls;
     // one CTA per (sequence, K / V head, key block); blocks past a sequence exit
     if ((rc = map_launch(launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, B * Hkv, d, causal != 0, bf16, st))))
         return rc;
-    DqConvertArgs c{};
-    c.dq_accum = dq_accum;
-    c.dq = dq;
-    c.elems = static_cast<long long>(total) * H * d;
-    c.scale = scale;
+    if (total == 0) return ATTN_OK;
     return map_launch(launch_dq_convert(c, bf16, st));
 }
 
@@ -877,6 +923,65 @@ int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void*
                         int Hkv, int d, int causal, float scale, void* stream) {
     return bwd_varlen_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, cu_seqlens, B, total,
                            max_seqlen, H, Hkv, d, causal, scale, stream, false);
+}
+
+int attn_fwd_varlen_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                       const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int total_q,
+                       int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
+                       int causal, float scale, void* stream) {
+    if (!cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, nullptr, lse, cu_seqlens_q, B, total_q, max_seqlen_q, H, Hkv,
+                           d, causal, scale, stream, true, {cu_seqlens_k, total_k, max_seqlen_k});
+}
+
+int attn_fwd_varlen_qk_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int total_q,
+                           int total_k, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
+                           int causal, float scale, void* stream) {
+    if (!cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, nullptr, lse, cu_seqlens_q, B, total_q, max_seqlen_q, H, Hkv,
+                           d, causal, scale, stream, false, {cu_seqlens_k, total_k, max_seqlen_k});
+}
+
+int attn_fwd_train_varlen_qk(const void* q, const void* k, const void* v, void* o, float* o32,
+                             float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                             int Hkv, int d, int causal, float scale, void* stream) {
+    if (!o32 || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, o32, lse, cu_seqlens_q, B, total_q, max_seqlen_q, H, Hkv, d,
+                           causal, scale, stream, true, {cu_seqlens_k, total_k, max_seqlen_k});
+}
+
+int attn_fwd_train_varlen_qk_f16(const void* q, const void* k, const void* v, void* o, float* o32,
+                                 float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                 int B, int total_q, int total_k, int max_seqlen_q,
+                                 int max_seqlen_k, int H, int Hkv, int d, int causal, float scale,
+                                 void* stream) {
+    if (!o32 || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return fwd_varlen_impl(q, k, v, o, o32, lse, cu_seqlens_q, B, total_q, max_seqlen_q, H, Hkv, d,
+                           causal, scale, stream, false, {cu_seqlens_k, total_k, max_seqlen_k});
+}
+
+int attn_bwd_varlen_qk(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                       void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                       int Hkv, int d, int causal, float scale, void* stream) {
+    if (!cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return bwd_varlen_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, cu_seqlens_q, B, total_q,
+                           max_seqlen_q, H, Hkv, d, causal, scale, stream, true,
+                           {cu_seqlens_k, total_k, max_seqlen_k});
+}
+
+int attn_bwd_varlen_qk_f16(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* D, float* dq_accum, void* dq, void* dk,
+                           void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                           int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                           int Hkv, int d, int causal, float scale, void* stream) {
+    if (!cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    return bwd_varlen_impl(q, k, v, dO, lse, D, dq_accum, dq, dk, dv, cu_seqlens_q, B, total_q,
+                           max_seqlen_q, H, Hkv, d, causal, scale, stream, false,
+                           {cu_seqlens_k, total_k, max_seqlen_k});
 }
 
 const char* attn_status_string(int s) {

@@ -485,7 +485,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Otherwise (dense, Hkv = H) the one query head of the same index, without
     // the divisions.  TMA head coordinates: kvc for K, V, dK, dV and qhead(it)
     // for Q, dO, dQ; qflat(it) is the (batch, head) index of the lse / D rows.
+    // N, tok0: the query rows; Nk, tokk0: the key rows (the same unless a packed
+    // batch gives keys of their own lengths), koff = Nk - N: with a causal mask
+    // key j is visible to query i iff j <= i + koff.
     int N = args.N, tok0 = 0, kvc = bkv, qc0 = bkv, qf0 = bkv, group = 1, split = 0;
+    int Nk = N, tokk0 = 0, koff = 0;
     bool varlen = false;
     if constexpr (GENERAL) {
         const int b = bkv / args.Hkv, kvh = bkv % args.Hkv;
@@ -504,14 +508,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int s1 = min(max(args.cu_seqlens[b + 1], s0), args.total);
             tok0 = s0;
             N = min(s1 - s0, args.max_seqlen);
+            tokk0 = tok0;
+            Nk = N;
+            if (args.cu_seqlens_k != nullptr) {
+                const int k0 = min(max(args.cu_seqlens_k[b], 0), args.total_k);
+                const int k1 = min(max(args.cu_seqlens_k[b + 1], k0), args.total_k);
+                tokk0 = k0;
+                Nk = min(k1 - k0, args.max_seqlen_k);
+                koff = Nk - N;
+            }
             kvc = kvh;
             qc0 = kvh * group;
-            if (j * kTile >= N) return;                             // not a block of this sequence
+            if (j * kTile >= Nk) return;                            // not a block of this sequence
         }
     }
-    const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks == key blocks
-    const int i_start = CAUSAL ? j : 0;
-    const int n_i = nq - i_start;                // query blocks per query head
+    const int nq = GENERAL ? (N + kTile - 1) / kTile : args.num_kvblocks;  // query blocks (dense: == key blocks)
+    // causal: the first query that sees key j * kTile is j * kTile - koff
+    const int i_start = !CAUSAL ? 0 : GENERAL ? max(0, j * kTile - koff) / kTile : j;
+    const int n_i = max(0, nq - i_start);        // query blocks per query head
     int n_it = group * n_i;
     // Block-sparse layout (dense, one query head per CTA): the query blocks
     // visited are those whose tile with key block j is kept, in order, listed
@@ -590,6 +604,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (n_it == 0) skip = true;
     }
+    if constexpr (GENERAL) {
+        if (varlen && n_it == 0 && !skip) {
+            // a packed sequence with keys but no queries: dK = dV = 0 for these keys
+            const int rows = min(kTile, Nk - j * kTile);
+            for (int e = threadIdx.x; e < rows * (D / 8); e += C::THREADS) {
+                const size_t rb = (static_cast<size_t>(tokk0 + j * kTile + e / (D / 8)) * args.Hkv + kvc) * D;
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.dk) + rb)[e % (D / 8)] = make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.dv) + rb)[e % (D / 8)] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (varlen && n_it == 0) skip = true;
+    }
 
     // Register budgets: 384 threads x 168 registers at launch; the role warps
     // (TMA, MMA, dQ reducer, lse/D loader) need few, the two compute
@@ -606,9 +632,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b) {
                         tma_load_3d(sbase + C::K_OFF + b * kBoxBytes, &tm_k, bar(C::B_KVFULL), b * kBoxCols,
-                                    tok0 + j * kTile, kvc, pol_kv);
+                                    tokk0 + j * kTile, kvc, pol_kv);
                         tma_load_3d(sbase + C::V_OFF + b * kBoxBytes, &tm_v, bar(C::B_KVFULL), b * kBoxCols,
-                                    tok0 + j * kTile, kvc, pol_kv);
+                                    tokk0 + j * kTile, kvc, pol_kv);
                     }
                     // Only the first STAGES Q / dO tiles: the dQ reducer reloads each
                     // stage itself as soon as its reductions have read it (see there).
@@ -795,7 +821,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
                 const float cs = args.scale_log2;
                 const uint64_t cs2 = f2_pack(cs, cs);
-                const bool key_ok = key < N;
+                const bool key_ok = key < Nk;
                 uint8_t* ds_row = smem + C::DS_OFF + c * kBoxBytes + r * 128;
                 float pv[64];        // P^T of this key row, query columns [64c, 64c + 64), fp32
                 // dropout: keep bits of this key row for query columns [64c + 32 ch, +32)
@@ -811,15 +837,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // per query: -lse*log2e (the loader stores it negated)
                     const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
                     const int qbase = i * kTile + 64 * c;
-                    // masking is needed only for keys past N and on the diagonal block
-                    const bool masked = !key_ok || (CAUSAL && i == j);
+                    // masking is needed only for keys past Nk and on blocks that cross
+                    // the causal boundary (first query + koff before the last key)
+                    const bool masked = !key_ok || (CAUSAL && (GENERAL ? i * kTile + koff < j * kTile + kTile - 1 : i == j));
                     uint32_t pp[32];
                     // two chunks of 32 query columns keep 32 S values live at a time
         #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
-                        // masked columns of this chunk are those below lim (the query
+                        // masked columns of this chunk are those below lim (query + koff
                         // precedes the key; all of them past the key tail)
-                        const int lim = key_ok ? key - (qbase + 32 * ch) : 32;
+                        const int lim = key_ok ? key - koff - (qbase + 32 * ch) : 32;
                         if constexpr (DROPOUT) {
                             // one generator call per lane and 16 query columns: patch
                             // (key patch of the lane's group, query patch), transposed so
@@ -971,11 +998,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // The last, partial key block of a packed sequence: a TMA box would
                     // also cover the first rows of the next sequence, so each thread
                     // stores its own key row (rows past the sequence are not written).
-                    const bool direct = varlen && (j + 1) * kTile > N;
+                    const bool direct = varlen && (j + 1) * kTile > Nk;
                     // fp32 output (written, or added to a running sum, row by row)
                     const bool f32out = GENERAL && args.dk32 != nullptr;
                     uint16_t* drow = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
-                                     (static_cast<size_t>(tok0 + j * kTile + r) * args.Hkv + kvc) * D;
+                                     (static_cast<size_t>(tokk0 + j * kTile + r) * args.Hkv + kvc) * D;
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
@@ -1028,7 +1055,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (ok && wq == 0 && lane == 0 && wait_bar(wc, bar(C::B_EPI + c), 0)) {
                         for (int b = 0; b < D / 64; ++b)
                             tma_store_3d(c == 0 ? &tm_dv : &tm_dk, sbase + region + b * kBoxBytes, 64 * b,
-                                         tok0 + j * kTile, kvc);
+                                         tokk0 + j * kTile, kvc);
                         bulk_commit_group();
                         bulk_wait_group_read<0>();   // shared memory read; writes complete with the kernel
                     }

@@ -51,6 +51,13 @@ struct FwdArgs {
     const int* cu_seqlens;
     int total;
     int max_seqlen;
+    // Keys of a different length (nullptr: the key rows of sequence b are its
+    // query rows): sequence b's keys / values are rows [cu_seqlens_k[b],
+    // cu_seqlens_k[b+1]) of the [total_k, Hkv, d] K and V, and with a causal
+    // mask key j is visible to query i iff j <= i + Lk - Lq (bottom-right).
+    const int* cu_seqlens_k;
+    int total_k;
+    int max_seqlen_k;
     // Block-sparse layout (nullptr: none): one byte per 128 x 128 tile
     // (query block, key block) at block_mask + bh * mask_head_stride, row-major
     // with mask_cols = ceil(N / 128) columns; zero drops the tile.
@@ -81,6 +88,11 @@ struct BwdArgs {
     const int* cu_seqlens;
     int total;
     int max_seqlen;
+    // keys of a different length as in FwdArgs (nullptr: same as the queries);
+    // K, V, dK, dV are then [total_k, Hkv, d]
+    const int* cu_seqlens_k;
+    int total_k;
+    int max_seqlen_k;
     // block-sparse layout as in FwdArgs (nullptr: none)
     const uint8_t* block_mask;
     long long mask_head_stride;

@@ -98,6 +98,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // length [total, H, d]: tok0 is the sequence's first token, N its length.
     int tok0 = 0, N = args.N, hq = bh;
     int hk = kv_head(bh, args.H, args.Hkv);                        // its K / V head
+    // Keys: Nk rows from token tokk0; causal offset koff = Nk - N (key j is
+    // visible to query i iff j <= i + koff).  Equal to the queries' unless a
+    // packed batch gives keys of their own lengths.
+    int tokk0 = 0, Nk = N, koff = 0;
     if constexpr (VARLEN) {
         const int b = bh / args.H, h = bh % args.H;
         const int s0 = min(max(args.cu_seqlens[b], 0), args.total);
@@ -108,14 +112,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         hk = h / (args.H / args.Hkv);
         qb = (N + C::TILES * kTile - 1) / (C::TILES * kTile) - 1 - rank;
         if (qb < 0) return;                                        // past this sequence
+        tokk0 = tok0;
+        Nk = N;
+        if (args.cu_seqlens_k != nullptr) {
+            const int k0 = min(max(args.cu_seqlens_k[b], 0), args.total_k);
+            const int k1 = min(max(args.cu_seqlens_k[b + 1], k0), args.total_k);
+            tokk0 = k0;
+            Nk = min(k1 - k0, args.max_seqlen_k);
+            koff = Nk - N;
+        }
     }
     const int q0 = qb * (C::TILES * kTile);
-    const int nkv_all = (N + kTile - 1) / kTile;
+    const int nkv_all = (Nk + kTile - 1) / kTile;
     int nkv[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int r0 = q0 + kTile * t;
-        nkv[t] = (r0 >= N) ? 0 : (CAUSAL ? min(nkv_all, r0 / kTile + 1) : nkv_all);
+        // causal: the tile's last row sees keys up to that row + koff
+        const int last_key = min(r0 + kTile, N) - 1 + koff;
+        nkv[t] = (r0 >= N) ? 0 : (CAUSAL ? (last_key < 0 ? 0 : min(nkv_all, last_key / kTile + 1)) : nkv_all);
     }
     int n_iter = max(nkv[0], nkv[1]);
 
@@ -199,6 +214,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (n_iter == 0) skip = true;
     }
+    if constexpr (VARLEN) {
+        if (n_iter == 0 && !skip) {
+            // no row of this CTA sees a key (keys of length 0, or a causal offset
+            // that leaves every row before the first key): O = 0, lse = -inf
+            const int rows = min(C::TILES * kTile, N - q0);
+            for (int e = threadIdx.x; e < rows * (D / 8); e += C::THREADS) {
+                const size_t rb = (static_cast<size_t>(tok0 + q0 + e / (D / 8)) * args.H + hq) * D;
+                reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + rb)[e % (D / 8)] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (TRAIN)
+                for (int e = threadIdx.x; e < rows * (D / 4); e += C::THREADS) {
+                    const size_t rb = (static_cast<size_t>(tok0 + q0 + e / (D / 4)) * args.H + hq) * D;
+                    reinterpret_cast<float4*>(args.o32 + rb)[e % (D / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            for (int e = threadIdx.x; e < rows; e += C::THREADS)
+                args.lse[static_cast<size_t>(bh) * args.max_seqlen + q0 + e] = -INFINITY;
+        }
+        if (n_iter == 0) skip = true;
+    }
 
     if (warp < 4) {
         if (skip) {
@@ -225,11 +259,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                    bar(C::B_KFULL + s), b * kBoxCols, tok0 + kblk(j) * kTile, hk, pol_kv);
+                                    bar(C::B_KFULL + s), b * kBoxCols, tokk0 + kblk(j) * kTile, hk, pol_kv);
                     mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
                     for (int b = 0; b < C::KBOX; ++b)
                         tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                    bar(C::B_VFULL + s), b * kBoxCols, tok0 + kblk(j) * kTile, hk, pol_kv);
+                                    bar(C::B_VFULL + s), b * kBoxCols, tokk0 + kblk(j) * kTile, hk, pol_kv);
                     issued = j + 1;
                 }
                 if (!ok) {
@@ -341,10 +375,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 float sv[128];
                 tmem_ld_sync(s_addr, sv);
-                // mask: key tail (keys >= N) and, on the diagonal block, keys > row
+                // mask: key tail (keys >= Nk) and, on the diagonal block, keys > row + koff
                 const int kb = kblk(j);
-                int limit = N - kb * kTile;
-                if (CAUSAL) limit = min(limit, row - kb * kTile + 1);
+                int limit = Nk - kb * kTile;
+                if (CAUSAL) limit = min(limit, row + koff - kb * kTile + 1);
                 if (limit < kTile) {
     #pragma unroll
                     for (int c = 0; c < kTile; ++c)
@@ -372,7 +406,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 // p = exp2(s tau log2e - m_ref), two columns per FMA / add instruction
                 const uint64_t cs2 = f2_pack(cs, cs);
-                const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+                // (packed batches: a row that sees no key keeps m_ref = -inf; its p
+                // must come out 0, not exp2(-inf + inf))
+                const float nm = (VARLEN && m_ref == -INFINITY) ? 0.f : -m_ref;
+                const uint64_t nm2 = f2_pack(nm, nm);
                 uint64_t sum2 = f2_pack(0.f, 0.f);
                 float sumb0 = 0.f, sumb1 = 0.f;
                 // TRAIN also sums the rounded p (two widening adds per pair);
@@ -457,7 +494,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // (block-sparse: a row whose kept tiles were all above the
                 // diagonal has an empty softmax, O = 0)
                 // (dropout: the kept weights are scaled by 256 / t)
-                const float inv_l = (SPARSE && !(den > 0.f)) ? 0.f
+                const float inv_l = ((SPARSE || VARLEN) && !(den > 0.f)) ? 0.f
                                     : (DROPOUT ? args.drop.drop_scale : 1.0f) / den;
                 const bool issuer = (warp & 3) == 0 && lane == 0;
                 const uint32_t stage = sbase + C::Q_OFF + t * C::TILE_BYTES;
@@ -557,7 +594,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // kernel, and waiting for them here kept the next CTA off the SM.
                 if (row < N)
                     args.lse[static_cast<size_t>(bh) * (VARLEN ? args.max_seqlen : N) + row] =
-                        ((SPARSE && !(l > 0.f)) ? -INFINITY : (m_ref + __log2f(l)) * kLn2);
+                        (((SPARSE || VARLEN) && !(l > 0.f)) ? -INFINITY : (m_ref + __log2f(l)) * kLn2);
+            }
+            if (VARLEN && ok && nkv[t] == 0 && row < N) {
+                // packed batch, keys shorter than the queries: every row of this tile
+                // precedes the first visible key (the other tile has work), O = 0,
+                // lse = -inf, each thread its own row
+                const size_t rbase = (static_cast<size_t>(tok0 + row) * args.H + hq) * D;
+                for (int c = 0; c < D; c += 8)
+                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + rbase + c) = make_uint4(0u, 0u, 0u, 0u);
+                if (TRAIN)
+                    for (int c = 0; c < D; c += 4)
+                        *reinterpret_cast<float4*>(args.o32 + rbase + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                args.lse[static_cast<size_t>(bh) * args.max_seqlen + row] = -INFINITY;
             }
         }
     }
