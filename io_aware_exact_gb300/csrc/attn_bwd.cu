@@ -830,13 +830,46 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 auto compute_p = [&](int it) -> bool {
                     const int s = it % C::STAGES;
                     const int i = qblk(it);
+                    const int qbase = i * kTile + 64 * c;
+                    if constexpr (DROPOUT) {
+                        // Keep bits of this key row for query columns [qbase, qbase + 64),
+                        // computed before S^T is waited for: the four generator calls
+                        // are independent chains that run while the tensor core works.
+                        // One call per lane and 16 query columns: patch (key patch of
+                        // the lane's group, query patch), transposed so that word b
+                        // holds key column b, then exchanged so that each lane holds
+                        // its key's bytes; bit q of kbits[ch] = query column 32 ch + q.
+                        const uint32_t kp = static_cast<uint32_t>((j * kTile + wq * 32) >> 2) + (lane >> 2);
+                        const uint32_t t4 = args.drop.drop_t * 0x01010101u;
+                        uint4 wv[4];
+        #pragma unroll
+                        for (int cg = 0; cg < 4; ++cg)      // cg = 2 ch + g
+                            wv[cg] = philox4x32_10(
+                                make_uint4(kp, static_cast<uint32_t>((qbase + 32 * (cg >> 1)) >> 2) + (lane & 3) + 4 * (cg & 1),
+                                           static_cast<uint32_t>(bkv), args.drop.offset),
+                                args.drop.seed_lo, args.drop.seed_hi);
+        #pragma unroll
+                        for (int ch = 0; ch < 2; ++ch) {
+                            uint32_t bits = 0u;
+        #pragma unroll
+                            for (int g = 0; g < 2; ++g) {
+                                uint32_t rv[4];
+                                exchange_patch_words(transpose_bytes(wv[2 * ch + g]), lane, rv);
+        #pragma unroll
+                                for (int cpp = 0; cpp < 4; ++cpp) {
+                                    const uint32_t m4 = __vcmpltu4(rv[cpp], t4) & 0x08040201u;
+                                    bits |= ((m4 * 0x01010101u) >> 24) << (16 * g + 4 * cpp);
+                                }
+                            }
+                            kbits[ch] = bits;
+                        }
+                    }
                     if (!__all_sync(0xffffffffu, wait_bar(wc, bar(C::B_SFULL), it & 1) &&
                                                      wait_bar(wc, bar(C::B_STFULL + s), (it / C::STAGES) & 1)))
                         return false;
                     tc_fence_after();
                     // per query: -lse*log2e (the loader stores it negated)
                     const float4* l2 = reinterpret_cast<const float4*>(stats + s * 2 * kTile + 64 * c);
-                    const int qbase = i * kTile + 64 * c;
                     // masking is needed only for keys past Nk and on blocks that cross
                     // the causal boundary (first query + koff before the last key)
                     const bool masked = !key_ok || (CAUSAL && (GENERAL ? i * kTile + koff < j * kTile + kTile - 1 : i == j));
@@ -847,30 +880,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // masked columns of this chunk are those below lim (query + koff
                         // precedes the key; all of them past the key tail)
                         const int lim = key_ok ? key - koff - (qbase + 32 * ch) : 32;
-                        if constexpr (DROPOUT) {
-                            // one generator call per lane and 16 query columns: patch
-                            // (key patch of the lane's group, query patch), transposed so
-                            // that word b holds key column b, then exchanged so that each
-                            // lane holds its key's bytes; bit q of kbits = query column q
-                            const uint32_t kp = static_cast<uint32_t>((j * kTile + wq * 32) >> 2) + (lane >> 2);
-                            const uint32_t t4 = args.drop.drop_t * 0x01010101u;
-                            uint32_t bits = 0u;
-        #pragma unroll
-                            for (int g = 0; g < 2; ++g) {
-                                const uint4 w = philox4x32_10(
-                                    make_uint4(kp, static_cast<uint32_t>((qbase + 32 * ch) >> 2) + (lane & 3) + 4 * g,
-                                               static_cast<uint32_t>(bkv), args.drop.offset),
-                                    args.drop.seed_lo, args.drop.seed_hi);
-                                uint32_t rv[4];
-                                exchange_patch_words(transpose_bytes(w), lane, rv);
-        #pragma unroll
-                                for (int cpp = 0; cpp < 4; ++cpp) {
-                                    const uint32_t m4 = __vcmpltu4(rv[cpp], t4) & 0x08040201u;
-                                    bits |= ((m4 * 0x01010101u) >> 24) << (16 * g + 4 * cpp);
-                                }
-                            }
-                            kbits[ch] = bits;
-                        }
                         uint32_t sr[32];
                         tmem_ld_sync(tmem + lane_off + C::S_COL + 64 * c + 32 * ch, sr);
         #pragma unroll
