@@ -51,9 +51,8 @@ struct FwdCfg {
     static constexpr int B_SFULL = B_KVEMPTY + STAGES;    // [2]
     static constexpr int B_PFULL = B_SFULL + 2;           // [2]
     static constexpr int B_OFULL = B_PFULL + 2;           // [2]
-    static constexpr int B_EPI_STAGED = B_OFULL + 2;      // [2] epilogue round staged (128 arrivals)
-    static constexpr int B_EPI_FREE = B_EPI_STAGED + 2;   // [2] epilogue round read by the TMA store
-    static constexpr int B_DRAIN = B_EPI_FREE + 2;
+    static constexpr int B_EPI_STAGED = B_OFULL + 2;      // [2] 16-bit O staged (128 arrivals)
+    static constexpr int B_DRAIN = B_EPI_STAGED + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + runtime alignment slack
@@ -171,7 +170,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(C::B_PFULL + t), 128);
             mbar_init(bar(C::B_OFULL + t), 1);
             mbar_init(bar(C::B_EPI_STAGED + t), 128);
-            mbar_init(bar(C::B_EPI_FREE + t), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
         // A failure recorded earlier on this device turns later CTAs into
@@ -184,7 +182,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_o);
-        if (TRAIN) tma_prefetch_desc(&tm_o32);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -477,12 +474,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(bar(C::B_PFULL + t));
             }
             // ------------------------------------------------------------ epilogue
-            // O leaves through the tile's Q buffer (free once the tile's last MMA has
-            // completed) in rounds of one Q-tile size, written out with TMA tensor
-            // stores: the fp32 O in two rounds (TRAIN), then the 16-bit O.  Each
-            // thread stages its row in the 128-byte-swizzled box layout; the
-            // warpgroup's first thread issues the stores once all rows are in and
-            // hands the buffer back when the stores have read it.
+            // The 16-bit O leaves through the tile's Q buffer (free once the tile's
+            // last MMA has completed), written out with TMA tensor stores: each
+            // thread stages its row in the 128-byte-swizzled box layout and the
+            // warpgroup's first thread issues the stores once all rows are in.  The
+            // fp32 O (TRAIN) goes straight from TMEM to global memory, read in the
+            // 16-lane x 256-bit shape so that every warp-wide store covers whole
+            // 32-byte sectors of the rows.
             if (ok && nkv[t] > 0) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_OFULL + t), 0));
             if (ok && nkv[t] > 0) {
                 tc_fence_after();
@@ -500,7 +498,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t stage = sbase + C::Q_OFF + t * C::TILE_BYTES;
                 uint8_t* stage_row = smem + C::Q_OFF + t * C::TILE_BYTES + r * 128;
                 const int row0 = q0 + kTile * t;
-                constexpr int ROUNDS = TRAIN ? 3 : 1;
                 if (VARLEN && row0 + kTile > N) {
                     // The last, partial tile of a sequence: a TMA box would also cover
                     // the first rows of the next sequence, so each thread stores its
@@ -532,60 +529,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     }
                 }
-                for (int k = 0; k < ROUNDS && ok && !(VARLEN && row0 + kTile > N); ++k) {
-                    const bool f32 = TRAIN && k < 2;
-                    if (k > 0) {
-                        ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_EPI_FREE + t), (k - 1) & 1));
-                        if (!ok) break;
-                    }
-                    if (f32) {
-                        // columns [k D/2, (k+1) D/2): boxes of 32 fp32 columns
+                if (ok && !(VARLEN && row0 + kTile > N)) {
+                    // all D columns of the 16-bit O: boxes of 64 columns
     #pragma unroll
-                        for (int c = 0; c < D / 2; c += 32) {
-                            uint32_t orr[32];
-                            tmem_ld_sync(o_addr + k * (D / 2) + c, orr);
-                            uint8_t* box_row = stage_row + (c / 32) * kBoxBytes;
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t orr[32];
+                        tmem_ld_sync(o_addr + c, orr);
+                        uint32_t pk[16];
     #pragma unroll
-                            for (int ch = 0; ch < 8; ++ch)
-                                *reinterpret_cast<float4*>(box_row + ((ch ^ (r & 7)) * 16)) =
-                                    make_float4(__uint_as_float(orr[4 * ch]) * inv_l,
-                                                __uint_as_float(orr[4 * ch + 1]) * inv_l,
-                                                __uint_as_float(orr[4 * ch + 2]) * inv_l,
-                                                __uint_as_float(orr[4 * ch + 3]) * inv_l);
-                        }
-                    } else {
-                        // all D columns: boxes of 64 16-bit columns
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                                __uint_as_float(orr[2 * e + 1]) * inv_l);
+                        uint8_t* box_row = stage_row + (c / 64) * kBoxBytes;
+                        const int ch0 = (c % 64) / 8;   // 16-byte chunks of this 32-column piece
     #pragma unroll
-                        for (int c = 0; c < D; c += 32) {
-                            uint32_t orr[32];
-                            tmem_ld_sync(o_addr + c, orr);
-                            uint32_t pk[16];
-    #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                pk[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv_l,
-                                                    __uint_as_float(orr[2 * e + 1]) * inv_l);
-                            uint8_t* box_row = stage_row + (c / 64) * kBoxBytes;
-                            const int ch0 = (c % 64) / 8;   // 16-byte chunks of this 32-column piece
-    #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4)
-                                *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
-                                    make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                        }
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            *reinterpret_cast<uint4*>(box_row + (((ch0 + v4) ^ (r & 7)) * 16)) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(bar(C::B_EPI_STAGED + t));
-                    if (issuer) {
-                        if (wait_bar(wc, bar(C::B_EPI_STAGED + t), k & 1)) {
-                            if (f32) {
-                                for (int b = 0; b < D / 64; ++b)
-                                    tma_store_3d(&tm_o32, stage + b * kBoxBytes, k * (D / 2) + 32 * b, tok0 + row0, hq);
-                            } else {
-                                for (int b = 0; b < D / 64; ++b)
-                                    tma_store_3d(&tm_o, stage + b * kBoxBytes, 64 * b, tok0 + row0, hq);
+                    if (issuer && wait_bar(wc, bar(C::B_EPI_STAGED + t), 0)) {
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_store_3d(&tm_o, stage + b * kBoxBytes, 64 * b, tok0 + row0, hq);
+                        bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                    }
+                }
+                if (TRAIN && ok && !(VARLEN && row0 + kTile > N)) {
+                    // fp32 O: thread t of the warp holds, per 16-lane half hh and
+                    // 64-column piece, rows 16 hh + t / 4 and 16 hh + t / 4 + 8 of the
+                    // warp's 32 at columns 2 (t % 4) + {0, 1} of each 8-column group;
+                    // the normaliser of a row comes from the thread that owns it
+    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+    #pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int src = 16 * hh + (lane >> 2) + 8 * rr;       // row within the warp
+                            const float inv = __shfl_sync(0xffffffffu, inv_l, src);
+                            const int grow = row0 + 32 * wq + src;
+                            float* dst = args.o32 +
+                                         (VARLEN ? (static_cast<size_t>(tok0 + grow) * args.H + hq) * D
+                                                 : (static_cast<size_t>(bh) * N + grow) * D) +
+                                         2 * (lane & 3);
+    #pragma unroll
+                            for (int cc = 0; cc < D; cc += 64) {
+                                uint32_t v[32];
+                                tmem_ld_16x256b_x8(tmem + (static_cast<uint32_t>(32 * wq + 16 * hh) << 16) +
+                                                       C::o_col(t) + cc, v);
+                                if (grow < N) {
+    #pragma unroll
+                                    for (int g = 0; g < 8; ++g)
+                                        *reinterpret_cast<float2*>(dst + cc + 8 * g) =
+                                            make_float2(__uint_as_float(v[4 * g + 2 * rr]) * inv,
+                                                        __uint_as_float(v[4 * g + 2 * rr + 1]) * inv);
+                                }
                             }
-                            bulk_commit_group();
-                            bulk_wait_group_read<0>();
-                            mbar_arrive(bar(C::B_EPI_FREE + t));
                         }
                     }
                 }
