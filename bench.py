@@ -744,6 +744,78 @@ def run_varlen(args):
     }))
 
 
+def run_varlen_qk(args):
+    """The training step on a packed batch whose keys have lengths of their
+    own: 32 sequences, each with Lq query tokens (uniform in [256, 2048]) that
+    attend, causally and aligned bottom-right, to Lk = Lq + a cached prefix
+    (uniform in [0, 6144]) keys; H = 16, d = 128, Q and K x3 (seeded).  FLOPs
+    count only the visible (query, key) pairs, 10 d per pair (the dense
+    causal step is 10 B H N^2 d / 2 in the same convention)."""
+    import torch
+    import numpy as np
+    import io_aware_exact_gb300 as attn
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(2468)
+    lq = rng.integers(256, 2049, size=32)
+    lk = lq + rng.integers(0, 6145, size=32)
+    H, d = 16, 128
+    Hkv = args.kv_heads or H
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    tq, tk, max_q, max_k = int(cu_q[-1]), int(cu_k[-1]), int(lq.max()), int(lk.max())
+    g = torch.Generator(device="cpu")
+    g.manual_seed(8642)
+    mk = lambda n, h, m: (torch.randn((n, h, d), generator=g) * m).to(torch.bfloat16).to(dev)
+    q, k, v, dO = mk(tq, H, 3.0), mk(tk, Hkv, 3.0), mk(tk, Hkv, 1.0), mk(tq, H, 1.0)
+    cq, ck = torch.from_numpy(cu_q).to(dev), torch.from_numpy(cu_k).to(dev)
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    o32 = torch.empty((tq, H, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((len(lq), H, max_q), dtype=torch.float32, device=dev)
+    D = torch.empty((tq, H), dtype=torch.float32, device=dev)
+    acc = torch.empty((tq, H, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        if ev:
+            ev[0].record(stream)
+        attn.forward_varlen(q, k, v, cq, max_q, True, scale, o=o, lse=lse, o32=o32, stream=stream,
+                            cu_seqlens_k=ck, max_seqlen_k=max_k)
+        if ev:
+            ev[2].record(stream)
+        attn.backward_varlen(q, k, v, o32, lse, dO, cq, max_q, True, scale, dq=dq, dk=dk, dv=dv,
+                             D=D, dq_accum=acc, stream=stream, cu_seqlens_k=ck, max_seqlen_k=max_k)
+        if ev:
+            ev[1].record(stream)
+
+    with ClockSampler(0) as clk:
+        evs = _timed_steps(stream, flush, step, args.steps, args.warmup, 3)
+    if attn.attn_get_device_status() != 0:
+        raise RuntimeError("device status set during the steps")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_fwd = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    # visible pairs of a sequence: query i sees keys 0 .. i + Lk - Lq
+    pairs = float(sum(int(a) * (int(b) - int(a)) + int(a) * (int(a) + 1) // 2 for a, b in zip(lq, lk)))
+    flops = 10.0 * d * H * pairs
+    peak = _peaks().get("bf16_tflops")
+    print(json.dumps({
+        "metric": "attention TFLOPS fwd+bwd, packed batch with keys of their own lengths (visible pairs only)",
+        "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1), Q and K x3)",
+        "config": {"workload": "varlen_qk_causal_32seq_q256to2048_prefix0to6144_h16_d128",
+                   "sequences": len(lq), "total_q": tq, "total_k": tk, "max_seqlen_q": max_q,
+                   "max_seqlen_k": max_k, "H": H, "kv_heads": Hkv, "d": d,
+                   "causal": "bottom-right", "l2": "L2 flushed (252 MB write) between steps"},
+        "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / peak, 4) if peak else None,
+        "fwd_train_ms": round(ms_fwd, 4), "bwd_ms": round(ms - ms_fwd, 4),
+        "clocks": clk.summary(),
+    }))
+
+
 def run_bsparse(args):
     """The training step (forward with fp32 O, D preprocess, backward) with a
     block-sparse layout on the causal B=2 H=16 N=8192 d=128 shape (Q and K
@@ -1040,6 +1112,9 @@ def main():
                          "every other workload's numbers under \"workloads\")")
     ap.add_argument("--varlen", action="store_true",
                     help="time the step on a packed variable-length batch instead")
+    ap.add_argument("--varlen-qk", action="store_true",
+                    help="time the step on a packed batch whose keys have lengths of their own "
+                         "(queries after a cached prefix) instead")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="time the step with dropout of this probability on P instead")
     ap.add_argument("--ring", type=int, default=0,
@@ -1053,6 +1128,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.varlen:
         run_varlen(args)
+    elif args.varlen_qk:
+        run_varlen_qk(args)
     elif args.bsparse > 0:
         run_bsparse(args)
     elif args.ring > 0:
