@@ -659,14 +659,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     constexpr uint32_t id_acc = idesc_f16(128, D, fmt, 0, 1);   // P^T x dO, dS^T x Q
                     constexpr uint32_t id_dq = idesc_f16(128, D, fmt, 1, 1);    // dS x K (both MN-major)
                     // S^T = K Q_i^T into the S columns, committed to SFULL
+                    const uint64_t k_kmaj = smem_desc(sbase + C::K_OFF, 16, 1024, LAYOUT_SW128);
+                    const uint64_t v_kmaj = smem_desc(sbase + C::V_OFF, 16, 1024, LAYOUT_SW128);
+                    const uint64_t k_mn = smem_desc(sbase + C::K_OFF, kBoxBytes, 1024, LAYOUT_SW128);
+                    const uint64_t ds_mn = smem_desc(sbase + C::DS_OFF, kBoxBytes, 1024, LAYOUT_SW128);
                     auto issue_s = [&](int it) {
-                        const uint32_t q_s = sbase + C::Q_OFF + (it % C::STAGES) * C::TILE_BYTES;
+                        const uint64_t q0 = smem_desc(sbase + C::Q_OFF + (it % C::STAGES) * C::TILE_BYTES, 16, 1024,
+                                                      LAYOUT_SW128);
         #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                            mma_ss(tmem + C::S_COL,
-                                   smem_desc(sbase + C::K_OFF + off, 16, 1024, LAYOUT_SW128),
-                                   smem_desc(q_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                            mma_ss(tmem + C::S_COL, desc_advance(k_kmaj, off), desc_advance(q0, off), id_kk, kk > 0);
                         }
                         mma_commit(bar(C::B_SFULL));
                     };
@@ -685,37 +688,34 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (it > 0 && !(ok = wait_bar(wc, bar(C::B_DQEMPTY), (it - 1) & 1))) break;
                         tc_fence_after();
                         // dP^T = V dO^T
+                        const uint64_t do_kmaj = smem_desc(do_s, 16, 1024, LAYOUT_SW128);
         #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                            mma_ss(tmem + C::DP_COL,
-                                   smem_desc(sbase + C::V_OFF + off, 16, 1024, LAYOUT_SW128),
-                                   smem_desc(do_s + off, 16, 1024, LAYOUT_SW128), id_kk, kk > 0);
+                            mma_ss(tmem + C::DP_COL, desc_advance(v_kmaj, off), desc_advance(do_kmaj, off), id_kk, kk > 0);
                         }
                         mma_commit(bar(C::B_DPFULL));
                         // dV += P^T dO   (K = the 128 queries of block i; query step kk
                         // lives with warpgroup kk / 4)
                         if (!(ok = wait_bar(wc, bar(C::B_PREADY), it & 1))) break;
                         tc_fence_after();
+                        const uint64_t do_mn = smem_desc(do_s, kBoxBytes, 1024, LAYOUT_SW128);
         #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_ts(tmem + C::DV_COL, tmem + C::P_COL + 64 * (kk >> 2) + 8 * (kk & 3),
-                                   smem_desc(do_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
-                                   (it > 0 || kk > 0) ? 1u : 0u);
+                                   desc_advance(do_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
                         // dK += dS^T Q
                         if (!(ok = wait_bar(wc, bar(C::B_DS), it & 1))) break;
                         tc_fence_after();
+                        const uint64_t q_mn = smem_desc(q_s, kBoxBytes, 1024, LAYOUT_SW128);
         #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + 64 * (kk >> 2) + 8 * (kk & 3),
-                                   smem_desc(q_s + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128), id_acc,
-                                   (it > 0 || kk > 0) ? 1u : 0u);
+                                   desc_advance(q_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
                         // dQ_i = dS K_j   (A = dS^T in smem read MN-major, B = K_j MN-major)
         #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss(tmem + C::DQ_COL,
-                                   smem_desc(sbase + C::DS_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
-                                   smem_desc(sbase + C::K_OFF + kk * 2048, kBoxBytes, 1024, LAYOUT_SW128),
+                            mma_ss(tmem + C::DQ_COL, desc_advance(ds_mn, kk * 2048), desc_advance(k_mn, kk * 2048),
                                    id_dq, kk > 0);
                         mma_commit(bar(C::B_DQFULL));
                     }

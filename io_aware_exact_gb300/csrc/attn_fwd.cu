@@ -37,7 +37,6 @@ template <int D>
 struct FwdCfg {
     static constexpr int TILES = 2;                       // 128-row Q tiles per CTA
     static constexpr int STAGES = (D == 128) ? 2 : 4;     // K/V ring depth
-    static constexpr int KBOX = D / kBoxCols;             // 64-column boxes per row
     static constexpr int TILE_BYTES = kTile * D * 2;      // one 128 x D tile
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + TILES * TILE_BYTES;
@@ -47,8 +46,12 @@ struct FwdCfg {
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_VFULL = B_KFULL + STAGES;
-    static constexpr int B_KVEMPTY = B_VFULL + STAGES;
-    static constexpr int B_SFULL = B_KVEMPTY + STAGES;    // [2]
+    // A K stage frees when the S MMAs of its block complete, a V stage when its
+    // PV MMAs do, one block later: separate barriers let the producer refill
+    // the K stage a whole block earlier than one shared barrier would.
+    static constexpr int B_KEMPTY = B_VFULL + STAGES;
+    static constexpr int B_VEMPTY = B_KEMPTY + STAGES;
+    static constexpr int B_SFULL = B_VEMPTY + STAGES;     // [2]
     static constexpr int B_PFULL = B_SFULL + 2;           // [2]
     static constexpr int B_OFULL = B_PFULL + 2;           // [2]
     static constexpr int B_EPI_STAGED = B_OFULL + 2;      // [2] 16-bit O staged (128 arrivals)
@@ -163,7 +166,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar(C::B_KFULL + s), 1);
             mbar_init(bar(C::B_VFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(C::B_SFULL + t), 1);
@@ -242,34 +246,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int ntiles = (nkv[1] > 0) ? 2 : 1;
                 mbar_arrive_expect_tx(bar(C::B_QFULL), ntiles * C::TILE_BYTES);
                 for (int t = 0; t < ntiles; ++t)
-                    for (int b = 0; b < C::KBOX; ++b)
-                        tma_load_3d(sbase + C::Q_OFF + t * C::TILE_BYTES + b * kBoxBytes, &tm_q,
-                                    bar(C::B_QFULL), b * kBoxCols, tok0 + q0 + kTile * t, hq, pol_q);
-                int issued = 0;
+                    tma_load_4d(sbase + C::Q_OFF + t * C::TILE_BYTES, &tm_q, bar(C::B_QFULL), 0,
+                                tok0 + q0 + kTile * t, 0, hq, pol_q);
+                // K_j and V_j, one copy each; K_j waits for its stage's K to be
+                // free, V_j for its V (the K stage frees first)
+                int issued_k = 0, issued_v = 0;
                 bool ok = true;
                 for (int j = 0; j < n_iter; ++j) {
                     const int s = j % C::STAGES;
-                    if (j >= C::STAGES) {
-                        ok = wait_bar(wc, bar(C::B_KVEMPTY + s), ((j / C::STAGES) - 1) & 1);
-                        if (!ok) break;
-                    }
+                    const uint32_t ph = ((j / C::STAGES) - 1) & 1;
+                    if (j >= C::STAGES && !(ok = wait_bar(wc, bar(C::B_KEMPTY + s), ph))) break;
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
-                    for (int b = 0; b < C::KBOX; ++b)
-                        tma_load_3d(sbase + C::K_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_k,
-                                    bar(C::B_KFULL + s), b * kBoxCols, tokk0 + kblk(j) * kTile, hk, pol_kv);
+                    tma_load_4d(sbase + C::K_OFF + s * C::TILE_BYTES, &tm_k, bar(C::B_KFULL + s), 0,
+                                tokk0 + kblk(j) * kTile, 0, hk, pol_kv);
+                    issued_k = j + 1;
+                    if (j >= C::STAGES && !(ok = wait_bar(wc, bar(C::B_VEMPTY + s), ph))) break;
                     mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
-                    for (int b = 0; b < C::KBOX; ++b)
-                        tma_load_3d(sbase + C::V_OFF + s * C::TILE_BYTES + b * kBoxBytes, &tm_v,
-                                    bar(C::B_VFULL + s), b * kBoxCols, tokk0 + kblk(j) * kTile, hk, pol_kv);
-                    issued = j + 1;
+                    tma_load_4d(sbase + C::V_OFF + s * C::TILE_BYTES, &tm_v, bar(C::B_VFULL + s), 0,
+                                tokk0 + kblk(j) * kTile, 0, hk, pol_kv);
+                    issued_v = j + 1;
                 }
                 if (!ok) {
                     // let copies already in flight land before the CTA's smem goes away
                     drain_wait(bar(C::B_QFULL), 0);
-                    for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+                    for (int j = max(0, issued_k - C::STAGES); j < issued_k; ++j)
                         drain_wait(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1);
+                    for (int j = max(0, issued_v - C::STAGES); j < issued_v; ++j)
                         drain_wait(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1);
-                    }
                 }
             }
         } else if (warp == 1) {
@@ -279,24 +282,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 constexpr uint32_t idesc_s = idesc_f16(128, 128, fmt, 0, 0);  // Q (K-major) x K (K-major)
                 constexpr uint32_t idesc_o = idesc_f16(128, D, fmt, 0, 1);    // P (TMEM) x V (MN-major)
                 auto issue_s = [&](int t, int s) {
+                    const uint64_t a0 = smem_desc(sbase + C::Q_OFF + t * C::TILE_BYTES, 16, 1024, LAYOUT_SW128);
+                    const uint64_t b0 = smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES, 16, 1024, LAYOUT_SW128);
     #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                        const uint64_t a = smem_desc(sbase + C::Q_OFF + t * C::TILE_BYTES + off, 16,
-                                                     1024, LAYOUT_SW128);
-                        const uint64_t b = smem_desc(sbase + C::K_OFF + s * C::TILE_BYTES + off, 16,
-                                                     1024, LAYOUT_SW128);
-                        mma_ss(tmem + C::s_col(t), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::s_col(t), desc_advance(a0, off), desc_advance(b0, off), idesc_s,
+                               kk > 0 ? 1u : 0u);
                     }
                 };
                 auto issue_pv = [&](int t, int s, bool acc) {
+                    const uint64_t b0 = smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES, kBoxBytes, 1024, LAYOUT_SW128);
     #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t b = smem_desc(sbase + C::V_OFF + s * C::TILE_BYTES + kk * 2048,
-                                                     kBoxBytes, 1024, LAYOUT_SW128);
-                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, b, idesc_o,
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, desc_advance(b0, kk * 2048), idesc_o,
                                (acc || kk > 0) ? 1u : 0u);
-                    }
                 };
                 bool ok = wait_bar(wc, bar(C::B_QFULL), 0) && wait_bar(wc, bar(C::B_KFULL + 0), 0);
                 if (ok) {
@@ -306,16 +306,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             issue_s(t, 0);
                             mma_commit(bar(C::B_SFULL + t));
                         }
+                    mma_commit(bar(C::B_KEMPTY + 0));   // K_0 read by both S MMAs
                 }
                 for (int j = 0; ok && j < n_iter; ++j) {
                     const int s = j % C::STAGES;
                     if (!(ok = wait_bar(wc, bar(C::B_VFULL + s), (j / C::STAGES) & 1))) break;
                     bool next_k_ready = false;
+                    const int t_last = (j < nkv[1]) ? 1 : 0;   // last tile that reads V_j
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= nkv[t]) continue;
                         if (!(ok = wait_bar(wc, bar(C::B_PFULL + t), j & 1))) break;
                         tc_fence_after();
                         issue_pv(t, s, j > 0);
+                        if (t == t_last) mma_commit(bar(C::B_VEMPTY + s));   // V_j read by its PV MMAs
                         if (j + 1 < nkv[t]) {
                             if (!next_k_ready) {
                                 const int s1 = (j + 1) % C::STAGES;
@@ -330,7 +333,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             mma_commit(bar(C::B_OFULL + t));
                         }
                     }
-                    mma_commit(bar(C::B_KVEMPTY + s));
+                    // K_{j+1} read by the S MMAs just issued
+                    if (next_k_ready) mma_commit(bar(C::B_KEMPTY + (j + 1) % C::STAGES));
                 }
                 // make sure no MMA is still reading smem / writing TMEM at teardown
                 mma_commit(bar(C::B_DRAIN));

@@ -149,6 +149,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// One whole 128-row tile through a 4-D tile map (coordinates: column within a
+// 64-column half, row, half, head): every 64-column half lands as its own
+// 128-byte-swizzled 16 KB box, the halves one after the other, in one copy.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
 // Store a shared-memory box to global memory through a tensor map (rows and
 // columns outside the tensor are not written).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
@@ -241,6 +254,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+
+// The descriptor of the operand `bytes` further on: the start address field
+// is the low 14 bits (address / 16) and shared addresses stay below 256 KB, so
+// no carry leaves the field.  The MMA warps issue 8 instructions per product
+// while sharing their SMSP with two busy softmax / compute warps; building
+// each descriptor once per product and advancing it per K step (one add
+// instead of a shift, mask and merge per operand) keeps the tensor core fed.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + (bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulation (32 bits):
