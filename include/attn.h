@@ -150,10 +150,9 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO,
 /*
  * Backward pass without caller-provided workspace (bf16).  The paper has no
  * counterpart: this entry point exists for callers that cannot allocate
- * device memory at the time of the call, for example code running while a
- * CUDA graph is captured (an allocation would invalidate the capture),
- * plug-ins whose host framework owns all allocations, or real-time programs
- * that allocate nothing after start-up.
+ * device memory at the time of the call, for example plug-ins whose host
+ * framework owns all allocations, or real-time programs that allocate
+ * nothing after start-up.
  *
  * Computes exactly what attn_bwd_preprocess followed by attn_bwd compute,
  * reading q, k, v, dO [B,H,N,d] and lse [B,H,N] and writing dq, dk, dv
@@ -164,8 +163,7 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* dO,
  *    e.g. B*H*N <= 32513 at d = 128 and <= 64527 at d = 64.  Larger problems
  *    return ATTN_ERR_SCRATCH_TOO_SMALL with nothing enqueued.
  *  - The first call on a device looks the array's device address up (once
- *    per device, with that device current); make that first call before
- *    capturing a stream into a graph.
+ *    per device, with that device current).
  *  - The looked-up address is kept for the life of the process, so calling
  *    this entry point on a device after a cudaDeviceReset of that device is
  *    not supported (see the shared conventions above).

@@ -2,10 +2,8 @@
 //
 // attn_bwd needs two workspaces besides its inputs and outputs: the row terms
 // D [B,H,N] and the fp32 dQ accumulator [B,H,N,d].  Some callers cannot
-// provide them: code that runs while a CUDA graph is being captured (where a
-// device allocation would break the capture), plug-ins whose host framework owns
-// every allocation and offers none to them, and real-time programs that must
-// not allocate after start-up.  attn_bwd_noalloc keeps both workspaces in one
+// provide them: plug-ins whose host framework owns every allocation and offers
+// none to them, and real-time programs that must not allocate after start-up.  attn_bwd_noalloc keeps both workspaces in one
 // file-scope device array of fixed size instead, so the caller passes only
 // its inputs and outputs.
 //

@@ -1,8 +1,8 @@
 """attn_bwd_noalloc: the backward pass for callers that cannot allocate.
 
-Callers that run inside a CUDA graph capture, inside a host framework that
-owns all device allocations, or in a real-time loop that allocates nothing
-after start-up cannot hand attn_bwd its D and dQ-accumulator workspaces.
+Callers that run inside a host framework that owns all device allocations,
+or in a real-time loop that allocates nothing after start-up, cannot hand
+attn_bwd its D and dQ-accumulator workspaces.
 attn_bwd_noalloc keeps those in a fixed 16 MiB device array inside the
 library.  These tests call it through the C ABI and check it against the
 regular attn_bwd_preprocess + attn_bwd path, twice in a row (the array is
