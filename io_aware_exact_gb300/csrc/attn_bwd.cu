@@ -993,9 +993,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int it = 0; ok && it < n_it; ++it)
                     ok = compute_p(it) && compute_ds(it) && readout_dq(it);
                 // ------------------------------------------------------------ epilogue: dV (c=0), dK (c=1)
-                // Rounded rows are staged in the 128-byte-swizzled box layout over the
-                // V (dV) or K (dK) tile, no longer read once every MMA has completed,
-                // and written out with TMA tensor stores by the warpgroup's first thread.
+                // At d = 128 the rounded rows are staged in the 128-byte-swizzled box
+                // layout over the V (dV) or K (dK) tile, no longer read once every MMA
+                // has completed, and written out with TMA tensor stores by the
+                // warpgroup's first thread; at d = 64 each thread stores its row.
                 if (ok) ok = __all_sync(0xffffffffu, wait_bar(wc, bar(C::B_ACC), 0));
                 if (ok) {
                     tc_fence_after();
@@ -1004,14 +1005,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t col = (c == 0) ? C::DV_COL : C::DK_COL;
                     const int region = (c == 0) ? C::V_OFF : C::K_OFF;
                     uint8_t* stage_row = smem + region + r * 128;
-                    // The last, partial key block of a packed sequence: a TMA box would
-                    // also cover the first rows of the next sequence, so each thread
-                    // stores its own key row (rows past the sequence are not written).
-                    const bool direct = varlen && (j + 1) * kTile > Nk;
+                    // Each thread stores its own key row from registers (rows past the
+                    // sequence are not written) for the last, partial key block of a
+                    // packed sequence, where a TMA box would also cover the first rows
+                    // of the next sequence, and always at d = 64, where these stores
+                    // running beside the last dQ reduce-adds beat queueing behind them
+                    // in the copy engine (at d = 128 the TMA stores are faster).
+                    const bool direct = D == 64 || (varlen && (j + 1) * kTile > Nk);
                     // fp32 output (written, or added to a running sum, row by row)
                     const bool f32out = GENERAL && args.dk32 != nullptr;
+                    const size_t krow = static_cast<size_t>(j) * kTile + r;
                     uint16_t* drow = static_cast<uint16_t*>(c == 0 ? args.dv : args.dk) +
-                                     (static_cast<size_t>(tokk0 + j * kTile + r) * args.Hkv + kvc) * D;
+                                     (varlen ? (static_cast<size_t>(tokk0) + krow) * args.Hkv + kvc
+                                             : static_cast<size_t>(kvc) * N + krow) * D;
         #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t a32[32];
